@@ -1,0 +1,346 @@
+"""Benchmark: paged MLA decode on GB300, one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload uniform] [--impl ours|reference]
+
+A step is one mla_decode call (split-KV kernel + reduction) over one synthetic
+decode batch resident in HBM.  L2 is flushed (a 256 MB device write, outside
+the timed events) before every timed step.  Under torchrun every rank decodes
+its own batch of the same shape (requests are independent: weak scaling, no
+collective on the data path); the step time is the maximum over ranks.
+
+--impl reference times the fp64 CPU oracle (the correctness reference) on a
+bounded sample of the same workload, on this host's cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_latent_attention_mla_gb300 import _native  # noqa: E402
+from paged_latent_attention_mla_gb300 import build as nbuild  # noqa: E402
+from paged_latent_attention_mla_gb300 import decoder_for  # noqa: E402
+from paged_latent_attention_mla_gb300 import workloads as wl  # noqa: E402
+from paged_latent_attention_mla_gb300.sharding import max_over_ranks, rank_seed  # noqa: E402
+
+METRIC = "MLA decode µs/call, TFLOP/s and KV HBM GB/s vs GB300 roofline fraction"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLOP_PER_KEY_HEAD = 2 * (576 + 512)  # QK^T over 576 dims + P.V over 512 dims
+
+
+def describe(prob) -> str:
+    w = prob.w
+    lens = prob.seq_lens.tolist()
+    klen = f"K={lens[0]}" if len(set(lens)) == 1 else f"K log-uniform [1,{w.max_len}] (sum {sum(lens)})"
+    extra = (" causal" if w.causal else "") + (f" window_left={w.window_left}" if w.window_left >= 0 else "")
+    return f"{w.name}: B={w.B} H={w.H} Sq={w.Sq} {klen}{extra} {w.dtype} page_size=64 pool={prob.pool_pages} pages"
+
+
+def algorithmic_counts(prob):
+    """FLOPs = 2*(576+512)*H*sum|vis(b,t)|; KV bytes = sum_b |union_t vis(b,t)| * 576 * elt."""
+    w = prob.w
+    elt = 1 if w.dtype == "e4m3" else 2
+    flops, kv = 0, 0
+    for K in prob.seq_lens.tolist():
+        lo_u, hi_u, vis = None, None, 0
+        for t in range(w.Sq):
+            hi = K - (w.Sq - 1 - t) if w.causal else K
+            lo = K - w.Sq - w.window_left + t if w.window_left >= 0 else 0
+            hi, lo = min(max(hi, 0), K), min(max(lo, 0), K)
+            lo = min(lo, hi)
+            vis += hi - lo
+            if hi > lo:
+                lo_u = lo if lo_u is None else min(lo_u, lo)
+                hi_u = hi if hi_u is None else max(hi_u, hi)
+        flops += FLOP_PER_KEY_HEAD * w.H * vis
+        if lo_u is not None:
+            kv += (hi_u - lo_u) * 576 * elt
+    return flops, kv
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(prob, budget_s: float = 12.0):
+    """The oracle as it stands, on this host's cores, over a bounded sample of rows."""
+    import oracle
+
+    p = prob.host_inputs()
+    total = prob.B * prob.Sq * prob.H
+    cores = oracle.max_threads()
+    rows = wl.sample_rows(prob, min(total, 4 * cores))
+    t0 = time.perf_counter()
+    oracle.decode(p, rows=rows)
+    dt = time.perf_counter() - t0
+    n = min(total, max(len(rows), int(len(rows) * budget_s / max(dt, 1e-3))))
+    if n > len(rows):
+        rows = wl.sample_rows(prob, n, seed=11)
+        t0 = time.perf_counter()
+        oracle.decode(p, rows=rows)
+        dt = time.perf_counter() - t0
+    flops = row_flops(prob, rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} of {total} (request, token, head) rows, every visible key, fp64 oracle, {dt:.2f} s",
+            "seconds": dt}
+
+
+def row_flops(prob, rows):
+    w = prob.w
+    lens = prob.seq_lens.tolist()
+    f = 0
+    for r in rows:
+        t = (r // w.H) % w.Sq
+        b = r // (w.H * w.Sq)
+        K = lens[b]
+        hi = K - (w.Sq - 1 - t) if w.causal else K
+        lo = K - w.Sq - w.window_left + t if w.window_left >= 0 else 0
+        hi, lo = min(max(hi, 0), K), min(max(lo, 0), K)
+        f += FLOP_PER_KEY_HEAD * max(0, hi - min(lo, hi))
+    return f
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    prob = wl.make_problem(args.workload)
+    flops, kv = algorithmic_counts(prob)
+    times = []
+    cb = None
+    per_step = min(args.ref_budget, 150.0 / max(1, args.warmup + args.steps))  # whole run within a few minutes
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(prob, budget_s=per_step)
+        if i >= args.warmup:
+            times.append(cb["seconds"])
+    v = cb["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(prob), "sample": cb["sample"]},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local_rank):
+    torch.cuda.set_device(local_rank)
+    nbuild.build()
+    _native.load()
+    prob = wl.make_problem(args.workload, seed=rank_seed(wl.WORKLOADS[args.workload].seed, rank))
+    d = prob.device_inputs("cuda")
+    dec = decoder_for(prob)
+    flops, kv = algorithmic_counts(prob)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty((prob.B, prob.Sq, prob.H, 512), dtype=dec.out_dtype, device="cuda")
+    lse = torch.empty((prob.B, prob.Sq, prob.H), dtype=torch.float32, device="cuda")
+
+    def step():
+        dec(d["q_latent"], d["q_rope"], d["ckv"], d["kpe"], d["page_table"], d["seq_lens"], d["scale"], out=out,
+            lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert dec.status() == _native.MLA_OK, "decode reported an error during warm-up"
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_max = max_over_ranks(ms)
+    launches = 2 * args.steps  # split-KV kernel + reduction per decode call
+
+    # end to end through the public API with host buffers: H2D of the step's queries,
+    # page table and lengths from pinned memory, decode, D2H of out and lse
+    hq = [d[k].cpu().pin_memory() for k in ("q_latent", "q_rope", "page_table", "seq_lens")]
+    dq = [torch.empty_like(d[k]) for k in ("q_latent", "q_rope", "page_table", "seq_lens")]
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in hq)
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        for h, dv in zip(hq, dq):
+            dv.copy_(h, non_blocking=True)
+        dec(dq[0], dq[1], d["ckv"], d["kpe"], dq[2], dq[3], d["scale"], out=out, lse=lse, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    e2e_ms = max_over_ranks(statistics.mean(e_ms))
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    tflops_rank = flops / (ms_max * 1e-3) / 1e12
+    kv_gbs = kv / (ms_max * 1e-3) / 1e9
+    t_hbm = kv / (peaks["hbm_gbs"] * 1e9)
+    # e4m3 contractions run at twice the bf16 tensor rate (nominal ratio 4.5 / 2.25 PFLOP/s)
+    tc_peak = peaks["bf16_tflops"] * (2.0 if prob.w.dtype == "e4m3" else 1.0)
+    t_tc = flops / (tc_peak * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": kv_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": kv_gbs / peaks["hbm_gbs"]}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops_rank, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": tflops_rank / tc_peak}
+    roof.update({"traffic": None, "kernel": "mla_decode (split-KV kernel + reduction, one call)",
+                 "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                 "t_roofline_us": 1e6 * max(t_hbm, t_tc)})
+    cb = cpu_baseline(prob, budget_s=args.cpu_budget) if args.cpu_budget > 0 else None
+    line = {
+        "metric": METRIC,
+        "value": tflops_rank * world,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "us_per_call": ms_max * 1e3,
+        "kv_gbs": kv_gbs * world,
+        "tflops": tflops_rank * world,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": prob.w.dtype,
+        "data": "synthetic",
+        "config": {"workload": describe(prob), "l2": "flushed before every timed step (256 MB device write)",
+                   "parallelism": f"{world} independent batches (one per GPU)", "flops_per_step": flops,
+                   "kv_bytes_per_step": kv},
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "cpu_baseline": ({k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")} if cb else None),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="uniform", choices=list(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
+    ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per reference-arm step")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, world, rank, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

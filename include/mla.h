@@ -1,0 +1,173 @@
+/*
+ * Paged Multi-Head Latent Attention (MLA) decode for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libmla_gb300.so.  The operation is the one the vLLM Kimi-K3
+ * kv_balanced_mla kernel page describes (BlackwellMultiHeadLatentAttentionForwardFP8,
+ * __call__ docstring and reduction_kernel): for every request b, query token
+ * t < seq_len_q and head h < H,
+ *
+ *   s_j = scale * (q_latent[b,t,h,:] . c_j + q_rope[b,t,h,:] . kpe_j)
+ *   out[b,t,h,:] = sum_j softmax(s)_j * c_j        (V is the latent c itself)
+ *   lse[b,t,h]   = log(sum_j exp(s_j))              (natural log)
+ *
+ * over the visible keys j of request b, fetched through the page table:
+ * key j lives in page page_table[b][j / page_size], slot j % page_size.
+ * Visible keys of token t (K = seq_lens[b], which counts the seq_len_q new
+ * tokens): j < K - (seq_len_q - 1 - t) when causal, else j < K (the softmax
+ * K bound); and j >= K - seq_len_q - window_left + t when window_left >= 0
+ * (the window_left docstring of __init__).  A row with no visible key gets
+ * out = 0 and lse = -inf (write_empty_output).
+ *
+ * Work is split along the KV axis across the GPU; each piece writes a
+ * normalized partial output and its log-sum-exp into the caller's workspace,
+ * and a reduction combines them with weights 2^(lse_i - lse) (reduction_kernel).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless marked host.  The caller owns every
+ *    buffer and the stream; the library allocates nothing and never
+ *    synchronizes the stream on the decode path.
+ *  - Errors are return codes.  Arguments are validated before anything is
+ *    launched; on any error nothing is launched and no output is touched.
+ *  - Tensors are dense and contiguous in the shapes given, and every pointer
+ *    is 16-byte aligned.
+ *  - Asynchronous CUDA faults surface as MLA_ERR_CUDA from a later call.
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,         /* a NULL / misaligned pointer, a bad size or shape */
+  MLA_ERR_UNSUPPORTED = 2,         /* valid, but outside what this build implements */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < what mla_plan reported */
+  MLA_ERR_CUDA = 4,                /* a CUDA runtime call failed (launch or an earlier fault) */
+  MLA_ERR_TIMEOUT = 5              /* a bounded device wait gave up (read by mla_workspace_status) */
+} mla_status_t;
+
+typedef enum { MLA_BF16 = 0, MLA_E4M3 = 1, MLA_F32 = 2 } mla_dtype_t;
+
+/*
+ * Tensor metadata the decode call needs beyond its pointers.
+ *  seq_len_q          query tokens per request (1 = plain decode; >1 = speculative block)
+ *  num_pages          pages in the cache pool (first dim of ckv / kpe)
+ *  page_table_stride  int32 entries per request row of page_table (its second dim)
+ *  qkv_dtype          MLA_BF16, or MLA_E4M3 (float8 e4m3fn) for q, ckv and kpe together
+ *  out_dtype          MLA_F32 or MLA_BF16 for out; lse is always fp32
+ *  causal             1: token t sees keys before K - (seq_len_q - 1 - t)
+ *  q_descale ...      per-tensor fp32 scales of the e4m3 inputs (value = code * descale);
+ *                     must be 1 for bf16 inputs.  The latent and rope parts of a key
+ *                     feed one contraction, so kpe_descale must equal ckv_descale
+ *                     (MLA_ERR_UNSUPPORTED otherwise): one scale for the key cache.
+ *  num_clusters       0: one persistent wave sized from the device (default);
+ *                     >0: use this many 2-CTA clusters (testing and partitioning)
+ */
+typedef struct {
+  int seq_len_q;
+  int num_pages;
+  int page_table_stride;
+  mla_dtype_t qkv_dtype;
+  mla_dtype_t out_dtype;
+  int causal;
+  float q_descale;
+  float ckv_descale;
+  float kpe_descale;
+  int num_clusters;
+} mla_config_t;
+
+/*
+ * Plan a decode batch (host only; reads the host copy of seq_lens).
+ *
+ * The KV range of every (request, token) row is cut into tiles of 256 keys;
+ * the visible tiles of all rows are laid end to end and dealt out in equal
+ * contiguous shares to a persistent wave of clusters, so unequal lengths
+ * balance (the page's get_split_kv / get_k_tile_count plan the same split per
+ * request; this plan splits the whole batch at once).  Tiles wholly below a
+ * sliding window are skipped.
+ *
+ *  seq_lens        host [B] int32, 0 <= seq_lens[b] <= page_table_stride * page_size
+ *  B, H            requests and heads, 1 <= H <= 128
+ *  page_size       keys per page: 64 (the only size this build supports)
+ *  window_left     -1 for full history, else >= 0
+ *  cfg             tensor metadata as above
+ *  split_kv        out: the most pieces any row is split into (1 = no reduction needed)
+ *  workspace_bytes out: device workspace mla_decode needs for this batch
+ *
+ * Returns MLA_ERR_CUDA when cfg->num_clusters == 0 and no device can be queried.
+ */
+MLA_API mla_status_t mla_plan(const int32_t *seq_lens, int B, int H, int page_size, int window_left, const mla_config_t *cfg,
+                      int *split_kv, size_t *workspace_bytes);
+
+/*
+ * Decode: out = softmax(q.[c;kpe]^T * scale).c and lse, for all B * seq_len_q * H rows.
+ *
+ *  q_latent   [B, seq_len_q, H, 512]   qkv_dtype
+ *  q_rope     [B, seq_len_q, H, 64]    qkv_dtype
+ *  ckv_cache  [num_pages, page_size, 512] qkv_dtype  (latent c, also the value)
+ *  kpe_cache  [num_pages, page_size, 64]  qkv_dtype  (rope key)
+ *  page_table [B, page_table_stride] int32; entries [0, ceil(seq_lens[b]/page_size))
+ *             must be page ids in [0, num_pages); later entries are never read
+ *  seq_lens   [B] int32, device copy of the lengths given to mla_plan
+ *  scale      softmax scale (e.g. 1/sqrt(576))
+ *  window_left -1, or the sliding-window span (same value as given to mla_plan)
+ *  out        [B, seq_len_q, H, 512] out_dtype
+ *  lse        [B, seq_len_q, H] fp32 natural-log LSE, or NULL to skip it
+ *  workspace  device scratch of at least the planned size, 256-byte aligned; its
+ *             contents need no initialization and are overwritten
+ *  stream     the CUDA stream all work is enqueued on
+ *
+ * Cache slots past a request's length and pages no visible key uses may hold
+ * any bits (NaN included) without affecting the result.
+ */
+MLA_API mla_status_t mla_decode(const void *q_latent, const void *q_rope, const void *ckv_cache, const void *kpe_cache,
+                        const int32_t *page_table, const int32_t *seq_lens, float scale, int window_left, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, cudaStream_t stream, int B, int H,
+                        int page_size, const mla_config_t *cfg);
+
+/*
+ * Debug gather: the decode kernel's page walk and tile load, written back densely.
+ *  dense_out [B, max_k, 576] elements of qkv_dtype: row j of request b is
+ *  (c_j | kpe_j) for j < seq_lens[b] and zero bytes for j >= seq_lens[b].
+ * Byte-for-byte equal to a host gather through the page table.
+ */
+MLA_API mla_status_t mla_debug_gather(const void *ckv_cache, const void *kpe_cache, const int32_t *page_table,
+                              const int32_t *seq_lens, int B, int page_size, int max_k, const mla_config_t *cfg,
+                              void *dense_out, cudaStream_t stream);
+
+/*
+ * Debug mask: the decode kernel's visibility rule, one bit per key.
+ *  bits [B, seq_len_q, ceil(max_k/32)] uint32: bit i of word w is set iff key
+ *  32*w + i is visible to that (request, token) row.
+ */
+MLA_API mla_status_t mla_debug_mask(const int32_t *seq_lens, int B, int window_left, int max_k, const mla_config_t *cfg,
+                            uint32_t *bits, cudaStream_t stream);
+
+/*
+ * Debug status: synchronizes the stream and reads the status word that the
+ * last mla_decode on this workspace left (MLA_OK, or MLA_ERR_TIMEOUT when a
+ * bounded device wait gave up).  Not for the decode path.
+ */
+MLA_API mla_status_t mla_workspace_status(const void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Static string naming a status code. */
+MLA_API const char *mla_status_string(mla_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

@@ -1,0 +1,281 @@
+// C ABI of the paged MLA decode library (declared in include/mla.h).
+//
+// Host-side work only: argument validation, the plan (a host mirror of the
+// device schedule, used to size the workspace), TMA descriptor encoding and
+// kernel launches.  Nothing here allocates device memory or synchronizes the
+// stream on the decode path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/mla.h"
+#include "mla_common.cuh"
+#include "mla_kernels.cuh"
+
+namespace mla {
+cudaError_t launch_split_kv_v0(const DecodeParams& p, cudaStream_t stream);
+}
+
+using namespace mla;
+
+namespace {
+
+constexpr int kMaxRows = 16384;   // B * seq_len_q (schedule scratch in shared memory)
+constexpr int kMaxSeqLenQ = 64;
+constexpr int kMaxSegments = 512;  // pieces one cluster may own
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status_t validate_cfg(const mla_config_t* cfg, int B, int H, int page_size, int window_left) {
+  if (!cfg) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || cfg->seq_len_q < 1 || cfg->num_pages < 1 || cfg->page_table_stride < 1) return MLA_ERR_INVALID_ARG;
+  if (window_left < -1 || cfg->num_clusters < 0) return MLA_ERR_INVALID_ARG;
+  if (cfg->qkv_dtype != MLA_BF16 && cfg->qkv_dtype != MLA_E4M3) return MLA_ERR_INVALID_ARG;
+  if (cfg->out_dtype != MLA_F32 && cfg->out_dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+  if (!(std::isfinite(cfg->q_descale) && std::isfinite(cfg->ckv_descale) && std::isfinite(cfg->kpe_descale)) ||
+      cfg->q_descale <= 0.f || cfg->ckv_descale <= 0.f || cfg->kpe_descale <= 0.f)
+    return MLA_ERR_INVALID_ARG;
+  if (cfg->qkv_dtype == MLA_BF16 && (cfg->q_descale != 1.f || cfg->ckv_descale != 1.f || cfg->kpe_descale != 1.f))
+    return MLA_ERR_INVALID_ARG;
+  // one scale for the whole key (latent and rope parts are one contraction)
+  if (cfg->qkv_dtype == MLA_E4M3 && cfg->ckv_descale != cfg->kpe_descale) return MLA_ERR_UNSUPPORTED;
+  if (H > kMaxHeads || page_size != kPageSize || cfg->seq_len_q > kMaxSeqLenQ) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * cfg->seq_len_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if ((long long)cfg->page_table_stride * kPageSize > (1ll << 30)) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+// clusters of one persistent wave on the current device (cached per device)
+int resolve_clusters(const mla_config_t* cfg, bool e4m3, int* out) {
+  if (cfg->num_clusters > 0) {
+    *out = cfg->num_clusters;
+    return 0;
+  }
+  static std::mutex mu;
+  static int cache[64][2];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> g(mu);
+  int& c = cache[dev][e4m3 ? 1 : 0];
+  if (c == 0) c = split_kv_max_clusters(dev, e4m3);
+  if (c <= 0) return -1;
+  *out = c;
+  return 0;
+}
+
+struct HostPlan {
+  int R, G, T, max_parts, max_segments;
+};
+
+// Host mirror of the device schedule (same functions, same integer arithmetic).
+HostPlan plan_rows(const int32_t* seq_lens, int B, int Sq, int causal, int window_left, int stride, int G) {
+  HostPlan hp{};
+  hp.R = B * Sq;
+  hp.G = G;
+  std::vector<long long> prefix(hp.R + 1, 0);
+  std::vector<int> n(hp.R, 0);
+  for (int r = 0; r < hp.R; ++r) {
+    int K = seq_lens[r / Sq];
+    K = K < 0 ? 0 : (K > stride * kPageSize ? stride * kPageSize : K);
+    int lo, hi, tlo, nt;
+    visible_range(K, Sq, r % Sq, causal, window_left, lo, hi);
+    tile_span(lo, hi, tlo, nt);
+    n[r] = nt;
+    prefix[r + 1] = prefix[r] + nt;
+  }
+  const long long T = prefix[hp.R];
+  hp.T = (int)T;
+  hp.max_parts = 0;
+  std::vector<int> segs(G, 0);
+  for (int r = 0; r < hp.R; ++r) {
+    if (n[r] == 0) continue;
+    const int cf = cluster_of_tile(prefix[r], T, G), cl = cluster_of_tile(prefix[r] + n[r] - 1, T, G);
+    if (cl - cf + 1 > hp.max_parts) hp.max_parts = cl - cf + 1;
+    for (int c = cf; c <= cl; ++c) segs[c]++;
+  }
+  hp.max_segments = 0;
+  for (int c = 0; c < G; ++c)
+    if (segs[c] > hp.max_segments) hp.max_segments = segs[c];
+  return hp;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over [d2][d1][d0] (d0 innermost, elements of es bytes), box {box0, box1, 1}
+bool encode3d(CUtensorMap* m, const void* base, bool e4m3, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+              uint32_t box1, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es = e4m3 ? 1 : 2;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_kv_maps(KvMaps* maps, const void* ckv, const void* kpe, const void* q_latent, const void* q_rope, bool e4m3,
+                    int num_pages, int rows_q, int H) {
+  const uint32_t blk = e4m3 ? 128 : 64;
+  const CUtensorMapSwizzle rope_sw = e4m3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  memset(maps, 0, sizeof(*maps));
+  bool ok = encode3d(&maps->ckv, ckv, e4m3, kDLatent, kPageSize, (uint64_t)num_pages, blk, kPageSize,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode3d(&maps->kpe, kpe, e4m3, kDRope, kPageSize, (uint64_t)num_pages, kDRope, kPageSize, rope_sw);
+  if (ok && q_latent)
+    ok = encode3d(&maps->q_latent, q_latent, e4m3, kDLatent, (uint64_t)H, (uint64_t)rows_q, blk, kRowsPerCta,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode3d(&maps->q_rope, q_rope, e4m3, kDRope, (uint64_t)H, (uint64_t)rows_q, kDRope, kRowsPerCta, rope_sw);
+  return ok;
+}
+
+mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+mla_status_t mla_plan(const int32_t* seq_lens, int B, int H, int page_size, int window_left, const mla_config_t* cfg,
+                      int* split_kv, size_t* workspace_bytes) {
+  if (!seq_lens || !split_kv || !workspace_bytes) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = validate_cfg(cfg, B, H, page_size, window_left);
+  if (st != MLA_OK) return st;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens[b] < 0 || (long long)seq_lens[b] > (long long)cfg->page_table_stride * kPageSize)
+      return MLA_ERR_INVALID_ARG;
+  int G;
+  if (resolve_clusters(cfg, cfg->qkv_dtype == MLA_E4M3, &G) != 0) return MLA_ERR_CUDA;
+  HostPlan hp = plan_rows(seq_lens, B, cfg->seq_len_q, cfg->causal, window_left, cfg->page_table_stride, G);
+  if (hp.max_segments > kMaxSegments) return MLA_ERR_UNSUPPORTED;
+  *split_kv = hp.max_parts < 1 ? 1 : hp.max_parts;
+  *workspace_bytes = ws_layout(hp.R, G).total;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode(const void* q_latent, const void* q_rope, const void* ckv_cache, const void* kpe_cache,
+                        const int32_t* page_table, const int32_t* seq_lens, float scale, int window_left, void* out,
+                        float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream, int B, int H,
+                        int page_size, const mla_config_t* cfg) {
+  mla_status_t st = validate_cfg(cfg, B, H, page_size, window_left);
+  if (st != MLA_OK) return st;
+  if (!q_latent || !q_rope || !ckv_cache || !kpe_cache || !page_table || !seq_lens || !out || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_latent) || !aligned16(q_rope) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
+      !aligned16(page_table) || !aligned16(seq_lens) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  const bool e4m3 = cfg->qkv_dtype == MLA_E4M3;
+  int G;
+  if (resolve_clusters(cfg, e4m3, &G) != 0) return MLA_ERR_CUDA;
+  const int R = B * cfg->seq_len_q;
+  if (workspace_bytes < ws_layout(R, G).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+
+  DecodeParams p{};
+  p.q_latent = q_latent;
+  p.q_rope = q_rope;
+  p.ckv = ckv_cache;
+  p.kpe = kpe_cache;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.lse = lse;
+  p.ws = static_cast<uint8_t*>(workspace);
+  p.B = B;
+  p.Sq = cfg->seq_len_q;
+  p.H = H;
+  p.num_pages = cfg->num_pages;
+  p.pt_stride = cfg->page_table_stride;
+  p.causal = cfg->causal ? 1 : 0;
+  p.window_left = window_left;
+  p.qkv_e4m3 = e4m3 ? 1 : 0;
+  p.out_f32 = cfg->out_dtype == MLA_F32 ? 1 : 0;
+  p.num_clusters = G;
+  p.scale = scale;
+  p.q_descale = cfg->q_descale;
+  p.ckv_descale = cfg->ckv_descale;
+  p.kpe_descale = cfg->kpe_descale;
+  p.score_scale_log2 = scale * cfg->q_descale * cfg->ckv_descale * 1.4426950408889634f;
+
+  cudaError_t e = launch_split_kv_v0(p, stream);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return cuda_status(launch_reduce(p, stream));
+}
+
+mla_status_t mla_debug_gather(const void* ckv_cache, const void* kpe_cache, const int32_t* page_table,
+                              const int32_t* seq_lens, int B, int page_size, int max_k, const mla_config_t* cfg,
+                              void* dense_out, cudaStream_t stream) {
+  mla_status_t st = validate_cfg(cfg, B, 1, page_size, -1);
+  if (st != MLA_OK) return st;
+  if (!ckv_cache || !kpe_cache || !page_table || !seq_lens || !dense_out || max_k < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(ckv_cache) || !aligned16(kpe_cache) || !aligned16(dense_out)) return MLA_ERR_INVALID_ARG;
+  const bool e4m3 = cfg->qkv_dtype == MLA_E4M3;
+  KvMaps maps;
+  if (!encode_kv_maps(&maps, ckv_cache, kpe_cache, nullptr, nullptr, e4m3, cfg->num_pages, 1, 1))
+    return MLA_ERR_CUDA;
+  return cuda_status(launch_debug_gather(maps, e4m3, page_table, seq_lens, B, cfg->page_table_stride, cfg->num_pages,
+                                         max_k, dense_out, nullptr, stream));
+}
+
+mla_status_t mla_debug_mask(const int32_t* seq_lens, int B, int window_left, int max_k, const mla_config_t* cfg,
+                            uint32_t* bits, cudaStream_t stream) {
+  mla_status_t st = validate_cfg(cfg, B, 1, kPageSize, window_left);
+  if (st != MLA_OK) return st;
+  if (!seq_lens || !bits || max_k < 1) return MLA_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_debug_mask(seq_lens, B, cfg->seq_len_q, cfg->causal ? 1 : 0, window_left, max_k, bits, stream));
+}
+
+mla_status_t mla_workspace_status(const void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!workspace || workspace_bytes < sizeof(WsHeader)) return MLA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (h.num_clusters <= 0 || h.num_rows <= 0) return MLA_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(h.num_rows, h.num_clusters);
+  if (workspace_bytes < L.total) return MLA_ERR_INVALID_ARG;
+  std::vector<uint32_t> words(2 * (size_t)h.num_clusters);
+  if (cudaMemcpy(words.data(), static_cast<const uint8_t*>(workspace) + L.cta_status, words.size() * 4,
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  uint32_t all = 0;
+  for (uint32_t w : words) all |= w;
+  if (all & kErrTimeout) return MLA_ERR_TIMEOUT;
+  if (all & (kErrBadPage | kErrBadLength)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+}  // extern "C"

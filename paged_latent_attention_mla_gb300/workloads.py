@@ -10,7 +10,7 @@ The five workloads are the decode shapes this library is measured on:
   tiny     B=2,   H=16,  Sq=1, K=[100, 257],        bf16, fp32 output
   uniform  B=64,  H=128, Sq=1, K=4096,              bf16
   varlen   B=128, H=128, Sq=1, K log-uniform [1, 32768] over a 2^18-page pool
-  fp8spec  B=32,  H=128, Sq=2 causal, K=16384,      float8 e4m3 with per-tensor scales
+  fp8spec  B=32,  H=128, Sq=2 causal, K=16384,      float8 e4m3: one scale for q, one for the key cache
   window   B=8,   H=128, Sq=4 causal, window_left=4096, K=131072, bf16
 
 Cache layout (vLLM paged MLA): ckv [num_pages, page_size, 512], kpe
@@ -209,10 +209,12 @@ def make_problem(w: Workload | str, *, seq_lens=None, seed=None, H=None, B=None,
         q_all = torch.cat([ql.reshape(-1), qr.reshape(-1)])
         _, qd = _quantize_e4m3(q_all)
         ql8, qr8 = (ql / qd).to(torch.float8_e4m3fn), (qr / qd).to(torch.float8_e4m3fn)
-        ckv8, cd = _quantize_e4m3(ckv)
-        kpe8, kd = _quantize_e4m3(kpe)
+        # one scale for the key cache: latent and rope parts of a key share it
+        kv_amax = max(float(ckv.abs().max()), float(kpe.abs().max()))
+        kd = kv_amax / 448.0 if kv_amax > 0 else 1.0
+        ckv8, kpe8 = (ckv / kd).to(torch.float8_e4m3fn), (kpe / kd).to(torch.float8_e4m3fn)
         ql, qr, ckv, kpe = ql8, qr8, ckv8, kpe8
-        descales = dict(q_descale=qd, ckv_descale=cd, kpe_descale=kd)
+        descales = dict(q_descale=qd, ckv_descale=kd, kpe_descale=kd)
     else:
         ql, qr, ckv, kpe = (t.to(torch.bfloat16) for t in (ql, qr, ckv, kpe))
 
