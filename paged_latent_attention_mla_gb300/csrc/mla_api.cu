@@ -92,6 +92,7 @@ HostPlan plan_rows(const int32_t* seq_lens, int B, int Sq, int causal, int windo
   const long long T = prefix[hp.R];
   hp.T = (int)T;
   hp.max_parts = 0;
+  G = deal_clusters(G, T);
   std::vector<int> segs(G, 0);
   for (int r = 0; r < hp.R; ++r) {
     if (n[r] == 0) continue;

@@ -31,8 +31,8 @@ constexpr uint32_t kErrBadLength = 4u;
 struct WsHeader {
   int32_t total_tiles;
   int32_t num_rows;
-  int32_t num_clusters;
-  int32_t pad;
+  int32_t num_clusters;   // clusters launched (the layout's G)
+  int32_t deal_clusters;  // clusters the tiles were dealt to
 };
 
 struct RowInfo {
@@ -101,6 +101,11 @@ __host__ __device__ inline int cluster_of_tile(long long x, long long T, long lo
 }
 
 __host__ __device__ inline long long cluster_tile_begin(long long c, long long T, long long G) { return c * T / G; }
+
+// clusters the T tiles are dealt to: never more than T, so none is empty
+__host__ __device__ inline int deal_clusters(int launched, long long T) {
+  return T < 1 ? 1 : (T < launched ? (int)T : launched);
+}
 
 // -------------------------------------------------------------- launch entry points (mla_kernels.cu)
 struct DecodeParams {

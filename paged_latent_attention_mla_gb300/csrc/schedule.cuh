@@ -4,7 +4,8 @@
 // Every (request, token) row r = b * Sq + t has visible keys [lo, hi) and the
 // KV tiles [tile_lo, tile_lo + n_r) that hold them.  The tiles of all rows are
 // laid end to end (row r's start is the prefix sum P_r) and dealt out in equal
-// contiguous shares to the G clusters of one persistent wave:
+// contiguous shares to G = min(clusters launched, T) clusters of one persistent
+// wave (so every dealing cluster owns at least one tile):
 // cluster c owns global tiles [floor(c*T/G), floor((c+1)*T/G)).
 // The piece of row r owned by cluster c writes partial slot r + c; a row owned
 // by a single cluster is written straight to the output.
@@ -24,7 +25,9 @@ struct RowWork {
 
 struct ScheduleView {
   const int32_t* prefix;  // [R + 1] in shared memory
-  int R, T, G;
+  int R, T;
+  int G;         // clusters the tiles are dealt to: min(launched, T), at least 1
+  int G_layout;  // clusters launched (sizes the workspace)
 };
 
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, uint32_t* err) {
@@ -94,7 +97,8 @@ __device__ inline ScheduleView build_schedule(const DecodeParams& p, int32_t* sc
   s.prefix = prefix;
   s.R = R;
   s.T = prefix[R];
-  s.G = p.num_clusters;
+  s.G_layout = p.num_clusters;
+  s.G = deal_clusters(p.num_clusters, s.T);
   return s;
 }
 
@@ -113,7 +117,7 @@ __device__ inline int row_of_tile(const ScheduleView& s, int x) {
 __device__ inline void cluster_rows(const ScheduleView& s, int c, int& first, int& last) {
   first = 1;
   last = 0;
-  if (s.T <= 0) return;
+  if (s.T <= 0 || c >= s.G) return;
   const long long b = cluster_tile_begin(c, s.T, s.G), e = cluster_tile_begin(c + 1, s.T, s.G);
   if (b >= e) return;
   first = row_of_tile(s, (int)b);
@@ -146,7 +150,7 @@ __device__ inline bool row_piece(const DecodeParams& p, const ScheduleView& s, i
 
 // Row table for the reduction (written once, by CTA 0 of the split-KV kernel).
 __device__ inline void write_row_table(const DecodeParams& p, const ScheduleView& s) {
-  const WsLayout L = ws_layout(s.R, s.G);
+  const WsLayout L = ws_layout(s.R, s.G_layout);
   RowInfo* info = reinterpret_cast<RowInfo*>(p.ws + L.row_info);
   for (int r = threadIdx.x; r < s.R; r += blockDim.x) {
     int lo, hi, tlo, n;
@@ -173,7 +177,8 @@ __device__ inline void write_row_table(const DecodeParams& p, const ScheduleView
     WsHeader* h = reinterpret_cast<WsHeader*>(p.ws);
     h->total_tiles = s.T;
     h->num_rows = s.R;
-    h->num_clusters = s.G;
+    h->num_clusters = s.G_layout;
+    h->deal_clusters = s.G;
   }
 }
 

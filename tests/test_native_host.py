@@ -50,7 +50,8 @@ def cfg(**kw):
 
 
 def host_plan(lens, Sq, causal, window, G, tile=256):
-    """Independent restatement of the batch deal: rows' visible tiles end to end, equal contiguous shares."""
+    """Independent restatement of the batch deal: the rows' visible tiles end to end, dealt in equal
+    contiguous shares to min(G, T) clusters; a row's pieces are the clusters whose share meets it."""
     rows = []
     for K in lens:
         for t in range(Sq):
@@ -60,14 +61,12 @@ def host_plan(lens, Sq, causal, window, G, tile=256):
             lo = min(lo, hi)
             rows.append(0 if hi <= lo else (hi + tile - 1) // tile - lo // tile)
     T = sum(rows)
-    bounds = [c * T // G for c in range(G + 1)]
+    Ge = max(1, min(G, T))
+    shares = [(c * T // Ge, (c + 1) * T // Ge) for c in range(Ge)]
+    assert all(e > b for b, e in shares) or T == 0
     parts, start = [], 0
     for nt in rows:
-        if nt == 0:
-            parts.append(0)
-            continue
-        owners = {c for c in range(G) for x in (start, start + nt - 1) if bounds[c] <= x < bounds[c + 1]}
-        parts.append(max(owners) - min(owners) + 1)
+        parts.append(sum(1 for b, e in shares if b < start + nt and start < e) if nt else 0)
         start += nt
     return len(rows), max([1] + parts)
 
