@@ -28,7 +28,7 @@ namespace {
 
 constexpr int kMaxRows = 16384;   // B * seq_len_q (schedule scratch in shared memory)
 constexpr int kMaxSeqLenQ = 64;
-constexpr int kMaxSegments = 512;  // pieces one cluster may own
+constexpr int kMaxSegments = 256;  // pieces one cluster may own (the split-KV kernel's segment list)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -231,7 +231,9 @@ mla_status_t mla_decode(const void* q_latent, const void* q_rope, const void* ck
   p.kpe_descale = cfg->kpe_descale;
   p.score_scale_log2 = scale * cfg->q_descale * cfg->ckv_descale * 1.4426950408889634f;
 
-  cudaError_t e = launch_split_kv_v0(p, stream);
+  KvMaps maps;
+  if (!encode_kv_maps(&maps, ckv_cache, kpe_cache, q_latent, q_rope, e4m3, cfg->num_pages, R, H)) return MLA_ERR_CUDA;
+  cudaError_t e = launch_split_kv(p, maps, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return cuda_status(launch_reduce(p, stream));
 }

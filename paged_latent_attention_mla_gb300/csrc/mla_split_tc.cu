@@ -1,0 +1,630 @@
+// Split-KV paged MLA decode on the tensor cores (tcgen05, 2-CTA clusters).
+//
+// One cluster = two CTAs on two SMs working on the same (request, token) row:
+// CTA r holds heads [64r, 64r + 64) of the 128-row M tile and the keys of its
+// two pages of every 256-key tile.  The leader CTA issues cta_group::2 MMAs:
+//   S[128 heads x 256 keys]  = Q[128 x 576] . [c | kpe]^T      (QK^T, K = 576)
+//   O[128 heads x 512 dims] += P[128 x 256] . c[256 x 512]      (V is c itself)
+// with S (two stages) and O in tensor memory.  Roles (12 warps per CTA):
+//   warps 0-3  softmax: online max / exp2 / row sums, P (bf16 or e4m3) to smem
+//   warps 4-7  correction: rescale O when the row max moves, final epilogue
+//   warp 8     MMA issue (leader CTA, one thread) and TMEM allocation
+//   warps 9-11 TMA loads of Q, K (two pages per CTA per tile), V (by page)
+// The split follows the batch schedule (schedule.cuh); a row owned by one
+// cluster is written to the output, other pieces to workspace partials that
+// the reduction kernel combines.  Every mbarrier wait is bounded: on timeout
+// the kernel records kErrTimeout, unwinds its roles, lets in-flight copies
+// land and frees TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "mla_common.cuh"
+#include "mla_kernels.cuh"
+#include "ptx.cuh"
+#include "schedule.cuh"
+#include "tma_pages.cuh"
+
+namespace mla {
+namespace tc {
+
+constexpr int kThreads = 384;
+constexpr int kMaxSegs = 256;
+// Rescale O only when a row's max grows by more than 2^8: P stays <= 256
+// (exact enough in bf16, below the e4m3 maximum of 448) and most tiles skip it.
+constexpr float kSkipCorrectionLog2 = 8.0f;
+
+template <bool E4M3>
+struct Cfg {
+  static constexpr int kBlk = E4M3 ? 128 : 64;  // elements per 128-byte column block
+  static constexpr int kNLat = kDLatent / kBlk;  // latent column blocks: 8 or 4
+  static constexpr int kNKb = kNLat + 1;         // QK^T contraction blocks (latent + rope)
+  static constexpr int kRopeSteps = E4M3 ? 2 : 4;
+  static constexpr uint32_t kQBytes = kNLat * 8192 + (E4M3 ? 4096 : 8192);
+  static constexpr int kPBytes = E4M3 ? 16384 : 32768;
+  static constexpr int kKStage = 16384;           // one K block of a tile: this CTA's 128 keys x 128 B
+  static constexpr int kVBlocks = E4M3 ? 2 : 4;   // this CTA's column blocks of V
+  static constexpr int kVStage = kVBlocks * 8192;  // one page (64 keys) of this CTA's V columns
+  static constexpr int kNK = E4M3 ? 4 : 3;
+  static constexpr int kNV = E4M3 ? 4 : 2;
+  static constexpr int kPvSteps = E4M3 ? 2 : 4;  // MMAs per page and output chunk (32 or 16 keys each)
+  static constexpr uint32_t kIdescQK = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 0);
+  static constexpr uint32_t kIdescPV = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 1);
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + kNKb * 8192;
+  static constexpr int kOffK = kOffP + kPBytes;
+  static constexpr int kOffV = kOffK + kNK * kKStage;
+  static constexpr int kOffSeg = kOffV + kNV * kVStage;
+  static constexpr int kOffMisc = kOffSeg + kMaxSegs * (int)sizeof(Segment);
+};
+
+struct Misc {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[4], v_empty[4];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t pv_ready, o_done, cor_ready, tail_bar, xchg_bar;
+  float xchg[2][128];             // per-tile row-max exchange between the two halves of a row
+  float xsum[128];                // final row-sum exchange
+  float corr[128];                // per-tile rescale factor, softmax -> correction
+  float fin_l[2][128], fin_m[2][128];  // final row statistics, double-buffered by segment
+  uint32_t tmem_base;
+  uint32_t err;
+  uint32_t abort;
+  int nseg;
+};
+
+template <bool E4M3>
+constexpr int smem_bytes() {
+  return Cfg<E4M3>::kOffMisc + (int)sizeof(Misc) + 1024;
+}
+static_assert(smem_bytes<false>() <= 232448, "bf16 kernel exceeds shared memory");
+static_assert(smem_bytes<true>() <= 232448, "e4m3 kernel exceeds shared memory");
+
+// bounded wait that also gives up when another role already aborted
+__device__ __forceinline__ bool kwait(Misc& M, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*reinterpret_cast<volatile uint32_t*>(&M.abort)) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        atomicOr(&M.err, kErrTimeout);
+        *reinterpret_cast<volatile uint32_t*>(&M.abort) = 1u;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+template <bool E4M3>
+__device__ __forceinline__ void store_p_chunk(uint8_t* sP, int row, int half, int ch, const float (&p)[32]) {
+  if constexpr (!E4M3) {
+    // keys [128 half + 32 ch, +32) of the row: P block 2 half + ch/2, bytes 64 (ch & 1) .. +64
+    uint8_t* blk = sP + (2 * half + (ch >> 1)) * 8192;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(p[8 * q + 2 * e], p[8 * q + 2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(blk + sw128_offset(row, 4 * (ch & 1) + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    // keys [128 half + 32 ch, +32): P block `half`, bytes 32 ch .. +32
+    uint8_t* blk = sP + half * 8192;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i0 = 16 * q + 4 * e;
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[i0], p[i0 + 1]), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[i0 + 2], p[i0 + 3]), __NV_SATFINITE, __NV_E4M3);
+        w[e] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(blk + sw128_offset(row, 2 * ch + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+template <bool E4M3>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    split_kv_tc(const __grid_constant__ DecodeParams p, const __grid_constant__ KvMaps maps) {
+  using C = Cfg<E4M3>;
+  constexpr int KIND = E4M3 ? 1 : 0;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Misc& M = *reinterpret_cast<Misc*>(smem + C::kOffMisc);
+  Segment* segs = reinterpret_cast<Segment*>(smem + C::kOffSeg);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t sQ = sbase + C::kOffQ, sP = sbase + C::kOffP, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cl = blockIdx.x >> 1;
+
+  if (tid == 0) {
+    M.err = 0;
+    M.abort = 0;
+  }
+  __syncthreads();
+  {
+    // the batch schedule, in the K/V ring memory before any tile lands there
+    int32_t* scratch = reinterpret_cast<int32_t*>(smem + C::kOffK);
+    ScheduleView sv = build_schedule(p, scratch, &M.err);
+    if (blockIdx.x == 0) write_row_table(p, sv);
+    if (tid == 0) M.nseg = build_segments(p, sv, cl, segs, kMaxSegs, &M.err);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_init(smem_addr(&M.q_full), 2);
+    mbar_init(smem_addr(&M.q_empty), 1);
+    for (int i = 0; i < C::kNK; ++i) {
+      mbar_init(smem_addr(&M.k_full[i]), 2);
+      mbar_init(smem_addr(&M.k_empty[i]), 1);
+    }
+    for (int i = 0; i < C::kNV; ++i) {
+      mbar_init(smem_addr(&M.v_full[i]), 2);
+      mbar_init(smem_addr(&M.v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&M.s_full[i]), 1);
+      mbar_init(smem_addr(&M.s_empty[i]), 8);  // 4 softmax warps x 2 CTAs
+    }
+    mbar_init(smem_addr(&M.pv_ready), 16);  // (4 softmax + 4 correction warps) x 2 CTAs
+    mbar_init(smem_addr(&M.o_done), 1);
+    mbar_init(smem_addr(&M.cor_ready), 4);
+    mbar_init(smem_addr(&M.tail_bar), 1);
+    mbar_init(smem_addr(&M.xchg_bar), 4);
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc<2>(smem_addr(&M.tmem_base), 512);
+    tmem_relinquish<2>();
+  }
+  if (warp == 9 && lane == 0) {
+    tma_prefetch_desc(&maps.ckv);
+    tma_prefetch_desc(&maps.kpe);
+    tma_prefetch_desc(&maps.q_latent);
+    tma_prefetch_desc(&maps.q_rope);
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+
+  const uint32_t tmem = M.tmem_base;
+  const int nseg = M.nseg;
+  auto lead = [&](uint64_t& bar) { return map_to_rank(smem_addr(&bar), 0); };
+  const float ln2 = 0.69314718055994530942f;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int L = tid, row = L & 63, half = L >> 6;
+    const uint32_t lanebase = static_cast<uint32_t>(warp * 32) << 16;
+    const float cl2 = p.score_scale_log2;
+    int j = 0;  // global tile counter of this cluster
+    uint32_t xph = 0;
+    bool ok = true;
+    for (int s = 0; s < nseg && ok; ++s) {
+      const Segment sg = segs[s];
+      int key_lo, key_hi;
+      visible_range(clamp_len(p, sg.row / p.Sq, nullptr), p.Sq, sg.row % p.Sq, p.causal, p.window_left, key_lo, key_hi);
+      const int n = sg.tile_end - sg.tile_begin;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int i = 0; i < n; ++i, ++j) {
+        const int st = j & 1;
+        if (!(ok = kwait(M, smem_addr(&M.s_full[st]), (j >> 1) & 1))) break;
+        tc_fence_after();
+        const int key0 = (sg.tile_begin + i) * kTileN + 128 * half;
+        const bool full = key0 >= key_lo && key0 + 128 <= key_hi;
+        const uint32_t sbase_t = tmem + lanebase + st * 128;
+        float mloc = -INFINITY;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(sbase_t + ch * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int k = key0 + ch * 32 + e;
+            const float v = (full || (k >= key_lo && k < key_hi)) ? u2f(r[e]) : -INFINITY;
+            mloc = fmaxf(mloc, v);
+          }
+        }
+        M.xchg[j & 1][L] = mloc;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&M.xchg_bar));
+        if (!(ok = kwait(M, smem_addr(&M.xchg_bar), xph & 1))) break;
+        ++xph;
+        const float mt = fmaxf(mloc, M.xchg[j & 1][L ^ 64]);
+        const float mts = mt * cl2;  // finite: every tile holds a visible key of the row
+        float m_new, fac;
+        if (i == 0) {
+          m_new = mts;
+          fac = 0.f;
+        } else if (mts > m_ref + kSkipCorrectionLog2) {
+          m_new = mts;
+          fac = exp2f(m_ref - m_new);
+        } else {
+          m_new = m_ref;
+          fac = 1.f;
+        }
+        l *= fac;
+        // the P buffer is free once the previous tile's P.V has completed
+        if (j > 0 && !(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(sbase_t + ch * 32, r);
+          tmem_ld_wait();
+          float pv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int k = key0 + ch * 32 + e;
+            const bool vis = full || (k >= key_lo && k < key_hi);
+            pv[e] = vis ? exp2f(fmaf(u2f(r[e]), cl2, -m_new)) : 0.f;
+            l += pv[e];
+          }
+          store_p_chunk<E4M3>(smem + C::kOffP, row, half, ch, pv);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_cluster(lead(M.s_empty[st]));
+          mbar_arrive_cluster(lead(M.pv_ready));
+        }
+        M.corr[L] = fac;
+        if (i == n - 1) {
+          // final row statistics: the two halves of the row add their sums
+          M.xsum[L] = l;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&M.xchg_bar));
+          if (!(ok = kwait(M, smem_addr(&M.xchg_bar), xph & 1))) break;
+          ++xph;
+          M.fin_l[s & 1][L] = l + M.xsum[L ^ 64];
+          M.fin_m[s & 1][L] = m_new;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&M.cor_ready));
+        m_ref = m_new;
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ correction + epilogue
+    const int L = tid - 128, row = L & 63, half = L >> 6;
+    const uint32_t lanebase = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t obase = tmem + lanebase + 256;
+    const WsLayout WL = ws_layout(p.B * p.Sq, p.num_clusters);
+    const int head = 64 * rank + row;
+    int j = 0;
+    bool ok = true;
+    for (int s = 0; s < nseg && ok; ++s) {
+      const Segment sg = segs[s];
+      const int n = sg.tile_end - sg.tile_begin;
+      for (int i = 0; i < n; ++i, ++j) {
+        if (!(ok = kwait(M, smem_addr(&M.cor_ready), j & 1))) break;
+        const float fac = M.corr[L];
+        if (i > 0 && __any_sync(0xffffffffu, fac != 1.f)) {
+          if (!(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[32];
+            tmem_ld32(obase + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(u2f(r[e]) * fac);
+            tmem_st32(obase + c * 32, r);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead(M.pv_ready));
+      }
+      if (!ok) break;
+      // epilogue: O / l to the output (whole row) or to the workspace partial
+      if (!(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
+      tc_fence_after();
+      const float lrow = M.fin_l[s & 1][L], mrow = M.fin_m[s & 1][L];
+      // P.V ran on the stored codes of c: the value scale (the key cache's descale) applies here
+      const float inv = p.ckv_descale / lrow;
+      const float lse2 = mrow + log2f(lrow);
+      const bool live = head < p.H;
+      const size_t orow = (size_t)sg.row * p.H + head;
+      const size_t slot = (size_t)sg.row + cl;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[32];
+        tmem_ld32(obase + c * 32, r);
+        tmem_ld_wait();
+        // TMEM columns [128 chunk, +128) of this lane hold D columns 256 chunk + 128 half + [0, 128)
+        const int d0 = 256 * (c >> 2) + 128 * half + 32 * (c & 3);
+        if (live) {
+          if (sg.whole) {
+            if (p.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDLatent + d0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv, u2f(r[4 * q + 2]) * inv,
+                                     u2f(r[4 * q + 3]) * inv);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * kDLatent + d0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  __nv_bfloat162 h2 = __floats2bfloat162_rn(u2f(r[8 * q + 2 * e]) * inv, u2f(r[8 * q + 2 * e + 1]) * inv);
+                  w[e] = *reinterpret_cast<uint32_t*>(&h2);
+                }
+                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.ws + WL.partial_o) +
+                                                    (slot * kHeadsPad + head) * kDLatent + d0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv, u2f(r[4 * q + 2]) * inv,
+                                   u2f(r[4 * q + 3]) * inv);
+          }
+        }
+      }
+      if (live && half == 0) {
+        if (sg.whole) {
+          if (p.lse) p.lse[orow] = lse2 * ln2;
+        } else {
+          reinterpret_cast<float*>(p.ws + WL.partial_lse)[slot * kHeadsPad + head] = lse2;
+        }
+      }
+      tc_fence_before();
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issue (leader CTA)
+    if (rank == 0 && lane == 0) {
+      int j = 0, pvc = 0, kfill = 0, vfill = 0;
+      bool ok = true;
+      auto qk = [&](int jt) -> bool {
+        const int st = jt & 1;
+        if (jt >= 2 && !kwait(M, smem_addr(&M.s_empty[st]), ((jt >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + st * 128;
+#pragma unroll 1
+        for (int kb = 0; kb < C::kNKb; ++kb) {
+          const int slot = kfill % C::kNK;
+          if (!kwait(M, smem_addr(&M.k_full[slot]), (kfill / C::kNK) & 1)) return false;
+          tc_fence_after();
+          const bool rope = kb == C::kNLat;
+          const int steps = rope ? C::kRopeSteps : 4;
+          const uint32_t qa = sQ + kb * 8192, ka = sK + slot * C::kKStage;
+          for (int t = 0; t < steps; ++t) {
+            uint64_t ad, bd;
+            if (E4M3 && rope) {
+              ad = smem_desc_sw64(qa + 32 * t, 512);
+              bd = smem_desc_sw64(ka + 32 * t, 512);
+            } else {
+              ad = smem_desc_sw128(qa + 32 * t, 16, 1024);
+              bd = smem_desc_sw128(ka + 32 * t, 16, 1024);
+            }
+            mma_ss<2, KIND>(d, ad, bd, C::kIdescQK, (kb | t) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair(smem_addr(&M.k_empty[slot]), 0x3);
+          ++kfill;
+        }
+        mma_commit_pair(smem_addr(&M.s_full[st]), 0x3);
+        return true;
+      };
+      auto pv = [&](bool first) -> bool {
+        if (!kwait(M, smem_addr(&M.pv_ready), pvc & 1)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int vp = 0; vp < 4; ++vp) {
+          const int slot = vfill % C::kNV;
+          if (!kwait(M, smem_addr(&M.v_full[slot]), (vfill / C::kNV) & 1)) return false;
+          tc_fence_after();
+          const uint32_t va = sV + slot * C::kVStage;
+          for (int t = 0; t < C::kPvSteps; ++t) {
+            const uint32_t pa = E4M3 ? sP + (vp >> 1) * 8192 + 64 * (vp & 1) + 32 * t : sP + vp * 8192 + 32 * t;
+            const uint64_t ad = smem_desc_sw128(pa, 16, 1024);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint32_t vb = E4M3 ? va + c * 8192 + t * 4096 : va + 2 * c * 8192 + t * 2048;
+              const uint64_t bd = smem_desc_sw128(vb, 8192, 1024);
+              mma_ss<2, KIND>(tmem + 256 + 128 * c, ad, bd, C::kIdescPV, (first && vp == 0 && t == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit_pair(smem_addr(&M.v_empty[slot]), 0x3);
+          ++vfill;
+        }
+        mma_commit_pair(smem_addr(&M.o_done), 0x3);
+        ++pvc;
+        return true;
+      };
+      for (int s = 0; s < nseg && ok; ++s) {
+        const int n = segs[s].tile_end - segs[s].tile_begin;
+        if (!(ok = kwait(M, smem_addr(&M.q_full), s & 1))) break;
+        tc_fence_after();
+        for (int i = 0; i < n && ok; ++i) {
+          ok = qk(j + i);
+          if (ok && i >= 1) ok = pv(i == 1);
+        }
+        if (!ok) break;
+        mma_commit_pair(smem_addr(&M.q_empty), 0x3);
+        ok = pv(n == 1);
+        j += n;
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ Q loads
+    if (lane == 0) {
+      for (int s = 0; s < nseg; ++s) {
+        if (s > 0 && !kwait(M, smem_addr(&M.q_empty), (s - 1) & 1)) break;
+        const uint32_t bar = lead(M.q_full);
+        mbar_arrive_expect_tx_cluster(bar, C::kQBytes);
+        const int row = segs[s].row;
+        for (int kb = 0; kb < C::kNLat; ++kb)
+          tma_load_3d_pair(sQ + kb * 8192, &maps.q_latent, kb * C::kBlk, 64 * rank, row, bar);
+        tma_load_3d_pair(sQ + C::kNLat * 8192, &maps.q_rope, 0, 64 * rank, row, bar);
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ K loads: this CTA's two pages of each tile
+    if (lane == 0) {
+      int kfill = 0;
+      bool ok = true;
+      for (int s = 0; s < nseg && ok; ++s) {
+        const Segment sg = segs[s];
+        const int b = sg.row / p.Sq;
+        const int npages = (clamp_len(p, b, nullptr) + kPageSize - 1) / kPageSize;
+        for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile) {
+          int pg[2];
+          for (int q = 0; q < 2; ++q) {
+            const int lp = 4 * tile + 2 * rank + q;
+            bool bad = false;
+            pg[q] = lp < npages ? page_of(p.page_table, p.pt_stride, p.num_pages, b, lp, bad) : p.num_pages;
+            if (bad) atomicOr(&M.err, kErrBadPage);
+          }
+          for (int kb = 0; kb < C::kNKb; ++kb) {
+            const int slot = kfill % C::kNK;
+            if (kfill >= C::kNK && !(ok = kwait(M, smem_addr(&M.k_empty[slot]), ((kfill / C::kNK) - 1) & 1))) break;
+            const bool rope = kb == C::kNLat;
+            const uint32_t bar = lead(M.k_full[slot]);
+            const uint32_t dst = sK + slot * C::kKStage;
+            if (!rope) {
+              mbar_arrive_expect_tx_cluster(bar, 2 * 8192);
+              for (int q = 0; q < 2; ++q) tma_load_3d_pair(dst + q * 8192, &maps.ckv, kb * C::kBlk, 0, pg[q], bar);
+            } else {
+              constexpr int rb = E4M3 ? 4096 : 8192;
+              mbar_arrive_expect_tx_cluster(bar, 2 * rb);
+              for (int q = 0; q < 2; ++q) tma_load_3d_pair(dst + q * rb, &maps.kpe, 0, 0, pg[q], bar);
+            }
+            ++kfill;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ V loads, one page (64 keys) per stage
+    int vfill = 0;
+    uint32_t tph = 0;
+    bool ok = true;
+    for (int s = 0; s < nseg && ok; ++s) {
+      const Segment sg = segs[s];
+      const int b = sg.row / p.Sq;
+      const int K = clamp_len(p, b, nullptr);
+      const int npages = (K + kPageSize - 1) / kPageSize;
+      const int tail_rows = K % kPageSize;
+      for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile) {
+        for (int vp = 0; vp < 4; ++vp) {
+          const int slot = vfill % C::kNV;
+          if (vfill >= C::kNV && !(ok = kwait(M, smem_addr(&M.v_empty[slot]), ((vfill / C::kNV) - 1) & 1))) break;
+          const int lp = 4 * tile + vp;
+          bool bad = false;
+          const int pg = lp < npages ? page_of(p.page_table, p.pt_stride, p.num_pages, b, lp, bad) : p.num_pages;
+          const bool tail = lp == npages - 1 && tail_rows != 0;
+          const uint32_t dst = sV + slot * C::kVStage;
+          if (!tail) {
+            if (lane == 0) {
+              if (bad) atomicOr(&M.err, kErrBadPage);
+              const uint32_t bar = lead(M.v_full[slot]);
+              mbar_arrive_expect_tx_cluster(bar, C::kVStage);
+              for (int u = 0; u < C::kVBlocks; ++u) {
+                const int gb = E4M3 ? 2 * u + (int)rank : 4 * (u >> 1) + 2 * (int)rank + (u & 1);
+                tma_load_3d_pair(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg, bar);
+              }
+            }
+          } else {
+            // last page of the request: land it here, zero the slots past its length, then hand it on
+            if (lane == 0) {
+              if (bad) atomicOr(&M.err, kErrBadPage);
+              mbar_arrive_expect_tx(smem_addr(&M.tail_bar), C::kVStage);
+              for (int u = 0; u < C::kVBlocks; ++u) {
+                const int gb = E4M3 ? 2 * u + (int)rank : 4 * (u >> 1) + 2 * (int)rank + (u & 1);
+                tma_load_3d(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg, smem_addr(&M.tail_bar));
+              }
+            }
+            __syncwarp();
+            if (!(ok = kwait(M, smem_addr(&M.tail_bar), tph & 1))) break;
+            ++tph;
+            for (int u = 0; u < C::kVBlocks; ++u) zero_block_rows(smem + C::kOffV + slot * C::kVStage + u * 8192, tail_rows, lane, 32);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lead(M.v_full[slot]));
+          }
+          __syncwarp();
+          ++vfill;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncwarp();
+  if (*reinterpret_cast<volatile uint32_t*>(&M.abort)) {
+    // let copies and MMAs already in flight finish before the memory goes away
+    for (int i = 0; i < 200; ++i) nanosleep_ns(1000);
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 8) tmem_dealloc<2>(tmem, 512);
+  if (tid == 0) {
+    const WsLayout WL = ws_layout(p.B * p.Sq, p.num_clusters);
+    reinterpret_cast<uint32_t*>(p.ws + WL.cta_status)[2 * cl + rank] = M.err;
+  }
+}
+
+}  // namespace tc
+
+cudaError_t launch_split_kv(const DecodeParams& p, const KvMaps& maps, cudaStream_t stream) {
+  const dim3 grid(2 * p.num_clusters), block(tc::kThreads);
+  if (p.qkv_e4m3) {
+    const int smem = tc::smem_bytes<true>();
+    cudaError_t e = cudaFuncSetAttribute(tc::split_kv_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    tc::split_kv_tc<true><<<grid, block, smem, stream>>>(p, maps);
+  } else {
+    const int smem = tc::smem_bytes<false>();
+    cudaError_t e = cudaFuncSetAttribute(tc::split_kv_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    tc::split_kv_tc<false><<<grid, block, smem, stream>>>(p, maps);
+  }
+  return cudaGetLastError();
+}
+
+int split_kv_max_clusters(int device, bool e4m3) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(tc::kThreads);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e;
+  if (e4m3) {
+    cfg.dynamicSmemBytes = tc::smem_bytes<true>();
+    cudaFuncSetAttribute(tc::split_kv_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+    e = cudaOccupancyMaxActiveClusters(&n, tc::split_kv_tc<true>, &cfg);
+  } else {
+    cfg.dynamicSmemBytes = tc::smem_bytes<false>();
+    cudaFuncSetAttribute(tc::split_kv_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+    e = cudaOccupancyMaxActiveClusters(&n, tc::split_kv_tc<false>, &cfg);
+  }
+  if (e != cudaSuccess || n <= 0) return sms / 2;
+  return n;
+}
+
+}  // namespace mla

@@ -169,12 +169,6 @@ __global__ void __launch_bounds__(kThreads) split_kv_v0(const DecodeParams p) {
 }
 }  // namespace v0
 
-int split_kv_max_clusters(int device, bool) {
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-  return sms / 2;
-}
-
 cudaError_t launch_split_kv_v0(const DecodeParams& p, cudaStream_t stream) {
   const int smem = (int)sizeof(v0::Smem);
   dim3 grid(2 * p.num_clusters);
