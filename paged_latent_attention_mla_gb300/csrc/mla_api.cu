@@ -18,10 +18,6 @@
 #include "mla_common.cuh"
 #include "mla_kernels.cuh"
 
-namespace mla {
-cudaError_t launch_split_kv_v0(const DecodeParams& p, cudaStream_t stream);
-}
-
 using namespace mla;
 
 namespace {
