@@ -139,6 +139,27 @@ MLA_API mla_status_t mla_decode(const void *q_latent, const void *q_rope, const 
                         int page_size, const mla_config_t *cfg);
 
 /*
+ * Decode without allocation: mla_decode with its scratch in a fixed array
+ * inside this library instead of a caller-provided workspace.  The pages this
+ * library follows have no counterpart of this call; it exists for callers that
+ * must not allocate device memory at all (code running under a runtime that
+ * owns all device memory once it serves, plugins given no allocator, paths that
+ * cannot afford an allocation's implicit synchronization).
+ *
+ * Same arguments and results as mla_decode, minus workspace and its size.
+ * The array is 64 MiB on every GPU that loads the library, held until the
+ * process exits; a batch needing more (see mla_plan's workspace_bytes) returns
+ * MLA_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call on a device
+ * looks the array's address up, so make it before any stream capture.  All
+ * calls share the one array: calls that overlap on the GPU race (serialize them,
+ * e.g. on one stream).  Nothing in it needs clearing between calls.
+ */
+MLA_API mla_status_t mla_decode_noalloc(const void *q_latent, const void *q_rope, const void *ckv_cache,
+                                        const void *kpe_cache, const int32_t *page_table, const int32_t *seq_lens,
+                                        float scale, int window_left, void *out, float *lse, cudaStream_t stream,
+                                        int B, int H, int page_size, const mla_config_t *cfg);
+
+/*
  * Debug gather: the decode kernel's page walk and tile load, written back densely.
  *  dense_out [B, max_k, 576] elements of qkv_dtype: row j of request b is
  *  (c_j | kpe_j) for j < seq_lens[b] and zero bytes for j >= seq_lens[b].

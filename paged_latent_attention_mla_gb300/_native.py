@@ -20,7 +20,8 @@ MLA_BF16, MLA_E4M3, MLA_F32 = 0, 1, 2
 
 _DTYPES = {torch.bfloat16: MLA_BF16, torch.float8_e4m3fn: MLA_E4M3, torch.float32: MLA_F32}
 
-EXPORTS = ("mla_plan", "mla_decode", "mla_debug_gather", "mla_debug_mask", "mla_workspace_status", "mla_status_string")
+EXPORTS = ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_debug_gather", "mla_debug_mask", "mla_workspace_status",
+           "mla_status_string")
 
 
 class MlaError(RuntimeError):
@@ -65,12 +66,14 @@ def load(path: str | None = None):
             cfgp = ctypes.POINTER(MlaConfig)
             lib.mla_plan.argtypes = [P, I, I, I, I, cfgp, ctypes.POINTER(I), ctypes.POINTER(S)]
             lib.mla_decode.argtypes = [P, P, P, P, P, P, F, I, P, P, P, S, P, I, I, I, cfgp]
+            lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, F, I, P, P, P, I, I, I, cfgp]
             lib.mla_debug_gather.argtypes = [P, P, P, P, I, I, I, cfgp, P, P]
             lib.mla_debug_mask.argtypes = [P, I, I, I, cfgp, P, P]
             lib.mla_workspace_status.argtypes = [P, S, P]
             lib.mla_status_string.argtypes = [I]
             lib.mla_status_string.restype = ctypes.c_char_p
-            for fn in ("mla_plan", "mla_decode", "mla_debug_gather", "mla_debug_mask", "mla_workspace_status"):
+            for fn in ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_debug_gather", "mla_debug_mask",
+                       "mla_workspace_status"):
                 getattr(lib, fn).restype = I
             _lib = lib
     return _lib
@@ -122,6 +125,16 @@ def mla_decode(q_latent, q_rope, ckv_cache, kpe_cache, page_table, seq_lens, sca
         _ptr(q_latent), _ptr(q_rope), _ptr(ckv_cache), _ptr(kpe_cache), _ptr(page_table), _ptr(seq_lens),
         float(scale), int(window_left), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream), int(B), int(H), int(page_size), ctypes.byref(cfg)))
+
+
+def mla_decode_noalloc(q_latent, q_rope, ckv_cache, kpe_cache, page_table, seq_lens, scale: float, window_left: int,
+                       out, lse, cfg: MlaConfig, stream=None):
+    """mla_decode with the library's own fixed scratch array: for callers that must not allocate."""
+    B, H = q_latent.shape[0], q_latent.shape[2]
+    _check("mla_decode_noalloc", load().mla_decode_noalloc(
+        _ptr(q_latent), _ptr(q_rope), _ptr(ckv_cache), _ptr(kpe_cache), _ptr(page_table), _ptr(seq_lens),
+        float(scale), int(window_left), _ptr(out), _ptr(lse), _stream(stream), int(B), int(H),
+        int(ckv_cache.shape[1]), ctypes.byref(cfg)))
 
 
 def mla_debug_gather(ckv_cache, kpe_cache, page_table, seq_lens, max_k: int, dense_out, cfg: MlaConfig, stream=None):
