@@ -9,7 +9,10 @@
 //   warps 0-3  softmax: online max / exp2 / row sums, P (bf16 or e4m3) to smem
 //   warps 4-7  correction: rescale O when the row max moves, final epilogue
 //   warp 8     MMA issue (leader CTA, one thread) and TMEM allocation
-//   warps 9-11 TMA loads of Q, K (two pages per CTA per tile), V (by page)
+//   warp 9     TMA loads of Q (once per piece of work)
+//   warp 10    TMA loads of K blocks and V pages into one ring of 16 KB slots,
+//              in exactly the order the MMAs consume them, page ids read a tile ahead
+//   warp 11    idle
 // The split follows the batch schedule (schedule.cuh); a row owned by one
 // cluster is written to the output, other pieces to workspace partials that
 // the reduction kernel combines.  Every mbarrier wait is bounded: on timeout
@@ -42,28 +45,30 @@ struct Cfg {
   static constexpr int kRopeSteps = E4M3 ? 2 : 4;
   static constexpr uint32_t kQBytes = kNLat * 8192 + (E4M3 ? 4096 : 8192);
   static constexpr int kPBytes = E4M3 ? 16384 : 32768;
-  static constexpr int kKStage = 16384;           // one K block of a tile: this CTA's 128 keys x 128 B
-  static constexpr int kVBlocks = E4M3 ? 2 : 4;   // this CTA's column blocks of V
-  static constexpr int kVStage = kVBlocks * 8192;  // one page (64 keys) of this CTA's V columns
-  static constexpr int kNK = E4M3 ? 4 : 3;
-  static constexpr int kNV = E4M3 ? 4 : 2;
+  // One ring of 16 KB slots holds, in consumption order, the K blocks of a tile (one
+  // slot each: this CTA's 128 keys x 128 B) and its V pages (this CTA's columns of 64
+  // keys: two slots in bf16, one per output chunk; one slot in e4m3).
+  static constexpr int kSlot = 16384;
+  static constexpr int kNS = E4M3 ? 10 : 7;
+  static constexpr int kVItems = E4M3 ? 1 : 2;    // ring slots per V page
   static constexpr int kPvSteps = E4M3 ? 2 : 4;  // MMAs per page and output chunk (32 or 16 keys each)
   static constexpr uint32_t kIdescQK = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 0);
   static constexpr uint32_t kIdescPV = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 1);
   static constexpr int kOffQ = 0;
   static constexpr int kOffP = kOffQ + kNKb * 8192;
-  static constexpr int kOffK = kOffP + kPBytes;
-  static constexpr int kOffV = kOffK + kNK * kKStage;
-  static constexpr int kOffSeg = kOffV + kNV * kVStage;
+  static constexpr int kOffRing = kOffP + kPBytes;
+  static constexpr int kOffSeg = kOffRing + kNS * kSlot;
   static constexpr int kOffMisc = kOffSeg + kMaxSegs * (int)sizeof(Segment);
 };
 
 struct Misc {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4];
-  uint64_t v_full[4], v_empty[4];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t pv_ready, o_done, cor_ready, tail_bar, xchg_bar;
+  uint64_t full[10], empty[10];  // ring slots
+  uint64_t s_full[2];
+  uint64_t pv_ready;    // leader: one arrival per CTA, P written and O corrected for the next P.V
+  uint64_t pv_local;    // this CTA's 4 softmax + 4 correction warps, forwarded to the leader's pv_ready
+  uint64_t tail_ready;  // leader: the peer zeroed the tail of a request's last page
+  uint64_t o_done, cor_ready, tail_bar, xchg_bar;
   float xchg[2][128];             // per-tile row-max exchange between the two halves of a row
   float xsum[128];                // final row-sum exchange
   float corr[128];                // per-tile rescale factor, softmax -> correction
@@ -99,6 +104,13 @@ __device__ __forceinline__ bool kwait(Misc& M, uint32_t bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// 2^x with the hardware approximation (relative error ~2^-22; denormal results flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <bool E4M3>
 __device__ __forceinline__ void store_p_chunk(uint8_t* sP, int row, int half, int ch, const float (&p)[32]) {
@@ -143,7 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   Misc& M = *reinterpret_cast<Misc*>(smem + C::kOffMisc);
   Segment* segs = reinterpret_cast<Segment*>(smem + C::kOffSeg);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t sQ = sbase + C::kOffQ, sP = sbase + C::kOffP, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
+  const uint32_t sQ = sbase + C::kOffQ, sP = sbase + C::kOffP, sRing = sbase + C::kOffRing;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const int cl = blockIdx.x >> 1;
@@ -154,29 +166,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   {
-    // the batch schedule, in the K/V ring memory before any tile lands there
-    int32_t* scratch = reinterpret_cast<int32_t*>(smem + C::kOffK);
+    // the batch schedule, in the ring memory before any tile lands there
+    int32_t* scratch = reinterpret_cast<int32_t*>(smem + C::kOffRing);
     ScheduleView sv = build_schedule(p, scratch, &M.err);
     if (blockIdx.x == 0) write_row_table(p, sv);
     if (tid == 0) M.nseg = build_segments(p, sv, cl, segs, kMaxSegs, &M.err);
   }
   __syncthreads();
   if (tid == 0) {
-    mbar_init(smem_addr(&M.q_full), 2);
+    mbar_init(smem_addr(&M.q_full), 1);  // armed by the leader with both CTAs' bytes
     mbar_init(smem_addr(&M.q_empty), 1);
-    for (int i = 0; i < C::kNK; ++i) {
-      mbar_init(smem_addr(&M.k_full[i]), 2);
-      mbar_init(smem_addr(&M.k_empty[i]), 1);
-    }
-    for (int i = 0; i < C::kNV; ++i) {
-      mbar_init(smem_addr(&M.v_full[i]), 2);
-      mbar_init(smem_addr(&M.v_empty[i]), 1);
+    for (int i = 0; i < C::kNS; ++i) {
+      mbar_init(smem_addr(&M.full[i]), 1);   // armed by the leader with both CTAs' bytes
+      mbar_init(smem_addr(&M.empty[i]), 1);  // the leader's MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&M.s_full[i]), 1);
-      mbar_init(smem_addr(&M.s_empty[i]), 8);  // 4 softmax warps x 2 CTAs
     }
-    mbar_init(smem_addr(&M.pv_ready), 16);  // (4 softmax + 4 correction warps) x 2 CTAs
+    mbar_init(smem_addr(&M.pv_ready), 2);
+    mbar_init(smem_addr(&M.pv_local), 8);
+    mbar_init(smem_addr(&M.tail_ready), 1);
     mbar_init(smem_addr(&M.o_done), 1);
     mbar_init(smem_addr(&M.cor_ready), 4);
     mbar_init(smem_addr(&M.tail_bar), 1);
@@ -224,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool full = key0 >= key_lo && key0 + 128 <= key_hi;
         const uint32_t sbase_t = tmem + lanebase + st * 128;
         float mloc = -INFINITY;
-#pragma unroll
+#pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t r[32];
           tmem_ld32(sbase_t + ch * 32, r);
@@ -249,7 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fac = 0.f;
         } else if (mts > m_ref + kSkipCorrectionLog2) {
           m_new = mts;
-          fac = exp2f(m_ref - m_new);
+          fac = ex2(m_ref - m_new);
         } else {
           m_new = m_ref;
           fac = 1.f;
@@ -257,7 +266,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l *= fac;
         // the P buffer is free once the previous tile's P.V has completed
         if (j > 0 && !(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
-#pragma unroll
+#pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t r[32];
           tmem_ld32(sbase_t + ch * 32, r);
@@ -267,7 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) {
             const int k = key0 + ch * 32 + e;
             const bool vis = full || (k >= key_lo && k < key_hi);
-            pv[e] = vis ? exp2f(fmaf(u2f(r[e]), cl2, -m_new)) : 0.f;
+            pv[e] = vis ? ex2(fmaf(u2f(r[e]), cl2, -m_new)) : 0.f;
             l += pv[e];
           }
           store_p_chunk<E4M3>(smem + C::kOffP, row, half, ch, pv);
@@ -275,10 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_cluster(lead(M.s_empty[st]));
-          mbar_arrive_cluster(lead(M.pv_ready));
-        }
+        if (lane == 0) mbar_arrive(smem_addr(&M.pv_local));
         M.corr[L] = fac;
         if (i == n - 1) {
           // final row statistics: the two halves of the row add their sums
@@ -326,7 +332,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(lead(M.pv_ready));
+        if (lane == 0) mbar_arrive(smem_addr(&M.pv_local));
+        if (warp == 4) {
+          // forward this CTA's readiness to the leader: one cross-CTA arrive per tile
+          if (!(ok = kwait(M, smem_addr(&M.pv_local), j & 1))) break;
+          if (lane == 0) mbar_arrive_cluster(lead(M.pv_ready));
+          __syncwarp();
+        }
       }
       if (!ok) break;
       // epilogue: O / l to the output (whole row) or to the workspace partial
@@ -389,21 +401,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue (leader CTA)
     if (rank == 0 && lane == 0) {
-      int j = 0, pvc = 0, kfill = 0, vfill = 0;
+      int j = 0, pvc = 0, fill = 0, tcount = 0;
+      int npages = 0, tail_rows = 0;  // of the current piece's request
       bool ok = true;
+      // next ring slot in consumption order: wait until both CTAs' data landed
+      auto take = [&](uint32_t& addr, int& slot) -> bool {
+        slot = fill % C::kNS;
+        if (!kwait(M, smem_addr(&M.full[slot]), (fill / C::kNS) & 1)) return false;
+        addr = sRing + slot * C::kSlot;
+        ++fill;
+        return true;
+      };
       auto qk = [&](int jt) -> bool {
+        // S stage jt & 1 was last read by the softmax of tile jt - 2, whose P.V was
+        // issued (after its pv_ready) before this QK^T: no separate wait
         const int st = jt & 1;
-        if (jt >= 2 && !kwait(M, smem_addr(&M.s_empty[st]), ((jt >> 1) - 1) & 1)) return false;
-        tc_fence_after();
         const uint32_t d = tmem + st * 128;
 #pragma unroll 1
         for (int kb = 0; kb < C::kNKb; ++kb) {
-          const int slot = kfill % C::kNK;
-          if (!kwait(M, smem_addr(&M.k_full[slot]), (kfill / C::kNK) & 1)) return false;
+          uint32_t ka;
+          int slot;
+          if (!take(ka, slot)) return false;
           tc_fence_after();
           const bool rope = kb == C::kNLat;
           const int steps = rope ? C::kRopeSteps : 4;
-          const uint32_t qa = sQ + kb * 8192, ka = sK + slot * C::kKStage;
+          const uint32_t qa = sQ + kb * 8192;
           for (int t = 0; t < steps; ++t) {
             uint64_t ad, bd;
             if (E4M3 && rope) {
@@ -415,49 +437,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             mma_ss<2, KIND>(d, ad, bd, C::kIdescQK, (kb | t) != 0 ? 1u : 0u);
           }
-          mma_commit_pair(smem_addr(&M.k_empty[slot]), 0x3);
-          ++kfill;
+          mma_commit_pair(smem_addr(&M.empty[slot]), 0x3);
         }
         mma_commit_pair(smem_addr(&M.s_full[st]), 0x3);
         return true;
       };
-      auto pv = [&](bool first) -> bool {
+      auto pv = [&](bool first, int tile) -> bool {
         if (!kwait(M, smem_addr(&M.pv_ready), pvc & 1)) return false;
         tc_fence_after();
 #pragma unroll 1
         for (int vp = 0; vp < 4; ++vp) {
-          const int slot = vfill % C::kNV;
-          if (!kwait(M, smem_addr(&M.v_full[slot]), (vfill / C::kNV) & 1)) return false;
+          // bf16: slot c holds the columns of output chunk c; e4m3: one slot holds both
+          uint32_t va[2];
+          int slot[2];
+          for (int it = 0; it < C::kVItems; ++it)
+            if (!take(va[it], slot[it])) return false;
+          if (4 * tile + vp == npages - 1 && tail_rows != 0) {
+            // the request's last page: the peer zeroed its slots' tail too
+            if (!kwait(M, smem_addr(&M.tail_ready), tcount & 1)) return false;
+            ++tcount;
+          }
           tc_fence_after();
-          const uint32_t va = sV + slot * C::kVStage;
           for (int t = 0; t < C::kPvSteps; ++t) {
             const uint32_t pa = E4M3 ? sP + (vp >> 1) * 8192 + 64 * (vp & 1) + 32 * t : sP + vp * 8192 + 32 * t;
             const uint64_t ad = smem_desc_sw128(pa, 16, 1024);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              const uint32_t vb = E4M3 ? va + c * 8192 + t * 4096 : va + 2 * c * 8192 + t * 2048;
+              const uint32_t vb = E4M3 ? va[0] + c * 8192 + t * 4096 : va[c] + t * 2048;
               const uint64_t bd = smem_desc_sw128(vb, 8192, 1024);
               mma_ss<2, KIND>(tmem + 256 + 128 * c, ad, bd, C::kIdescPV, (first && vp == 0 && t == 0) ? 0u : 1u);
             }
           }
-          mma_commit_pair(smem_addr(&M.v_empty[slot]), 0x3);
-          ++vfill;
+          for (int it = 0; it < C::kVItems; ++it) mma_commit_pair(smem_addr(&M.empty[slot[it]]), 0x3);
         }
         mma_commit_pair(smem_addr(&M.o_done), 0x3);
         ++pvc;
         return true;
       };
       for (int s = 0; s < nseg && ok; ++s) {
-        const int n = segs[s].tile_end - segs[s].tile_begin;
+        const Segment sg = segs[s];
+        const int n = sg.tile_end - sg.tile_begin;
+        const int K = clamp_len(p, sg.row / p.Sq, nullptr);
+        npages = (K + kPageSize - 1) / kPageSize;
+        tail_rows = K % kPageSize;
         if (!(ok = kwait(M, smem_addr(&M.q_full), s & 1))) break;
         tc_fence_after();
         for (int i = 0; i < n && ok; ++i) {
           ok = qk(j + i);
-          if (ok && i >= 1) ok = pv(i == 1);
+          if (ok && i >= 1) ok = pv(i == 1, sg.tile_begin + i - 1);
         }
         if (!ok) break;
         mma_commit_pair(smem_addr(&M.q_empty), 0x3);
-        ok = pv(n == 1);
+        ok = pv(n == 1, sg.tile_end - 1);
         j += n;
       }
     }
@@ -467,7 +498,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int s = 0; s < nseg; ++s) {
         if (s > 0 && !kwait(M, smem_addr(&M.q_empty), (s - 1) & 1)) break;
         const uint32_t bar = lead(M.q_full);
-        mbar_arrive_expect_tx_cluster(bar, C::kQBytes);
+        // the leader arms the barrier with both CTAs' bytes; the peer's copies only complete bytes on it
+        if (rank == 0) mbar_arrive_expect_tx(smem_addr(&M.q_full), 2 * C::kQBytes);
         const int row = segs[s].row;
         for (int kb = 0; kb < C::kNLat; ++kb)
           tma_load_3d_pair(sQ + kb * 8192, &maps.q_latent, kb * C::kBlk, 64 * rank, row, bar);
@@ -475,93 +507,111 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 10) {
-    // ------------------------------------------------------------ K loads: this CTA's two pages of each tile
-    if (lane == 0) {
-      int kfill = 0;
-      bool ok = true;
-      for (int s = 0; s < nseg && ok; ++s) {
-        const Segment sg = segs[s];
-        const int b = sg.row / p.Sq;
-        const int npages = (clamp_len(p, b, nullptr) + kPageSize - 1) / kPageSize;
-        for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile) {
-          int pg[2];
-          for (int q = 0; q < 2; ++q) {
-            const int lp = 4 * tile + 2 * rank + q;
-            bool bad = false;
-            pg[q] = lp < npages ? page_of(p.page_table, p.pt_stride, p.num_pages, b, lp, bad) : p.num_pages;
-            if (bad) atomicOr(&M.err, kErrBadPage);
-          }
-          for (int kb = 0; kb < C::kNKb; ++kb) {
-            const int slot = kfill % C::kNK;
-            if (kfill >= C::kNK && !(ok = kwait(M, smem_addr(&M.k_empty[slot]), ((kfill / C::kNK) - 1) & 1))) break;
-            const bool rope = kb == C::kNLat;
-            const uint32_t bar = lead(M.k_full[slot]);
-            const uint32_t dst = sK + slot * C::kKStage;
-            if (!rope) {
-              mbar_arrive_expect_tx_cluster(bar, 2 * 8192);
-              for (int q = 0; q < 2; ++q) tma_load_3d_pair(dst + q * 8192, &maps.ckv, kb * C::kBlk, 0, pg[q], bar);
-            } else {
-              constexpr int rb = E4M3 ? 4096 : 8192;
-              mbar_arrive_expect_tx_cluster(bar, 2 * rb);
-              for (int q = 0; q < 2; ++q) tma_load_3d_pair(dst + q * rb, &maps.kpe, 0, 0, pg[q], bar);
-            }
-            ++kfill;
-          }
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ V loads, one page (64 keys) per stage
-    int vfill = 0;
+    // ------------------------------------------------------------ K blocks and V pages, one ring
+    // Consumption order of each piece: K(t0), then K(t), V(t - 1) for the following tiles,
+    // then V(last); a K block is this CTA's two pages x 128 B of columns, a V page this CTA's
+    // output columns of one page.
+    int fill = 0;
     uint32_t tph = 0;
     bool ok = true;
+    // wait for the next free slot (lane-uniform)
+    auto acquire = [&](int& slot) -> bool {
+      slot = fill % C::kNS;
+      if (fill >= C::kNS && !kwait(M, smem_addr(&M.empty[slot]), ((fill / C::kNS) - 1) & 1)) return false;
+      ++fill;
+      return true;
+    };
     for (int s = 0; s < nseg && ok; ++s) {
       const Segment sg = segs[s];
       const int b = sg.row / p.Sq;
       const int K = clamp_len(p, b, nullptr);
       const int npages = (K + kPageSize - 1) / kPageSize;
       const int tail_rows = K % kPageSize;
-      for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile) {
-        for (int vp = 0; vp < 4; ++vp) {
-          const int slot = vfill % C::kNV;
-          if (vfill >= C::kNV && !(ok = kwait(M, smem_addr(&M.v_empty[slot]), ((vfill / C::kNV) - 1) & 1))) break;
-          const int lp = 4 * tile + vp;
+      auto page_ids = [&](int tile, int (&pg)[4]) {
+        for (int q = 0; q < 4; ++q) {
+          const int lp = 4 * tile + q;
           bool bad = false;
-          const int pg = lp < npages ? page_of(p.page_table, p.pt_stride, p.num_pages, b, lp, bad) : p.num_pages;
-          const bool tail = lp == npages - 1 && tail_rows != 0;
-          const uint32_t dst = sV + slot * C::kVStage;
-          if (!tail) {
-            if (lane == 0) {
-              if (bad) atomicOr(&M.err, kErrBadPage);
-              const uint32_t bar = lead(M.v_full[slot]);
-              mbar_arrive_expect_tx_cluster(bar, C::kVStage);
-              for (int u = 0; u < C::kVBlocks; ++u) {
-                const int gb = E4M3 ? 2 * u + (int)rank : 4 * (u >> 1) + 2 * (int)rank + (u & 1);
-                tma_load_3d_pair(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg, bar);
-              }
+          pg[q] = lp < npages ? page_of(p.page_table, p.pt_stride, p.num_pages, b, lp, bad) : p.num_pages;
+          if (bad && lane == 0) atomicOr(&M.err, kErrBadPage);
+        }
+      };
+      auto load_k = [&](int tile, const int (&pg)[4]) -> bool {
+        for (int kb = 0; kb < C::kNKb; ++kb) {
+          int slot;
+          if (!acquire(slot)) return false;
+          if (lane == 0) {
+            const bool rope = kb == C::kNLat;
+            const uint32_t bar = lead(M.full[slot]);
+            const uint32_t dst = sRing + slot * C::kSlot;
+            const int rb = rope && E4M3 ? 4096 : 8192;
+            if (rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot]), 4 * rb);  // both CTAs' two pages
+            for (int q = 0; q < 2; ++q) {
+              const int page = pg[2 * rank + q];
+              if (!rope) tma_load_3d_pair(dst + q * rb, &maps.ckv, kb * C::kBlk, 0, page, bar);
+              else tma_load_3d_pair(dst + q * rb, &maps.kpe, 0, 0, page, bar);
             }
-          } else {
-            // last page of the request: land it here, zero the slots past its length, then hand it on
-            if (lane == 0) {
-              if (bad) atomicOr(&M.err, kErrBadPage);
-              mbar_arrive_expect_tx(smem_addr(&M.tail_bar), C::kVStage);
-              for (int u = 0; u < C::kVBlocks; ++u) {
-                const int gb = E4M3 ? 2 * u + (int)rank : 4 * (u >> 1) + 2 * (int)rank + (u & 1);
-                tma_load_3d(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg, smem_addr(&M.tail_bar));
-              }
-            }
-            __syncwarp();
-            if (!(ok = kwait(M, smem_addr(&M.tail_bar), tph & 1))) break;
-            ++tph;
-            for (int u = 0; u < C::kVBlocks; ++u) zero_block_rows(smem + C::kOffV + slot * C::kVStage + u * 8192, tail_rows, lane, 32);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead(M.v_full[slot]));
           }
           __syncwarp();
-          ++vfill;
+        }
+        return true;
+      };
+      auto load_v = [&](int tile, const int (&pg)[4]) -> bool {
+        for (int vp = 0; vp < 4; ++vp) {
+          int slot[2];
+          for (int it = 0; it < C::kVItems; ++it)
+            if (!acquire(slot[it])) return false;
+          const bool tail = 4 * tile + vp == npages - 1 && tail_rows != 0;
+          // this CTA's 128-byte column blocks of V: bf16 blocks {0,1,4,5} or {2,3,6,7}
+          // (two per slot, one slot per output chunk), e4m3 blocks {rank, 2 + rank}
+          if (lane == 0) {
+            const uint32_t tbar = smem_addr(&M.tail_bar);
+            if (tail) mbar_arrive_expect_tx(tbar, C::kVItems * C::kSlot);
+            for (int it = 0; it < C::kVItems; ++it) {
+              const uint32_t dst = sRing + slot[it] * C::kSlot;
+              const uint32_t bar = lead(M.full[slot[it]]);
+              if (!tail && rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot[it]]), 2 * C::kSlot);
+              for (int u = 0; u < 2; ++u) {
+                const int gb = E4M3 ? 2 * u + (int)rank : 4 * it + 2 * (int)rank + u;
+                if (tail) tma_load_3d(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg[vp], tbar);
+                else tma_load_3d_pair(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg[vp], bar);
+              }
+            }
+          }
+          __syncwarp();
+          if (tail) {
+            // last page of the request: each CTA lands it locally and zeroes the slots past
+            // its length; the leader then completes its slots' phases, the peer reports on
+            // tail_ready (the MMA waits for both on this page)
+            if (!kwait(M, smem_addr(&M.tail_bar), tph & 1)) return false;
+            ++tph;
+            for (int it = 0; it < C::kVItems; ++it)
+              for (int u = 0; u < 2; ++u)
+                zero_block_rows(smem + C::kOffRing + slot[it] * C::kSlot + u * 8192, tail_rows, lane, 32);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0)
+                for (int it = 0; it < C::kVItems; ++it) mbar_arrive(smem_addr(&M.full[slot[it]]));
+              else
+                mbar_arrive_cluster(lead(M.tail_ready));
+            }
+            __syncwarp();
+          }
+        }
+        return true;
+      };
+      int pg_prev[4], pg_cur[4], pg_next[4];
+      page_ids(sg.tile_begin, pg_cur);
+      for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile) {
+        if (tile + 1 < sg.tile_end) page_ids(tile + 1, pg_next);  // read a tile ahead
+        ok = load_k(tile, pg_cur);
+        if (ok && tile > sg.tile_begin) ok = load_v(tile - 1, pg_prev);
+        for (int q = 0; q < 4; ++q) {
+          pg_prev[q] = pg_cur[q];
+          pg_cur[q] = pg_next[q];
         }
       }
+      if (ok) ok = load_v(sg.tile_end - 1, pg_prev);
     }
   }
 
