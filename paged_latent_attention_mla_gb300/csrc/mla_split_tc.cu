@@ -232,19 +232,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int key0 = (sg.tile_begin + i) * kTileN + 128 * half;
         const bool full = key0 >= key_lo && key0 + 128 <= key_hi;
         const uint32_t sbase_t = tmem + lanebase + st * 128;
-        float mloc = -INFINITY;
+        // visible keys of this thread's 128: [vlo, vhi) relative to key0 (all of them on most
+        // tiles); the mask is one unsigned compare, so the loops stay branch-free
+        const int vlo = full ? 0 : min(max(key_lo - key0, 0), 128);
+        const int vhi = full ? 128 : min(max(key_hi - key0, 0), 128);
+        const uint32_t vspan = static_cast<uint32_t>(vhi - vlo);
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t r[32];
           tmem_ld32(sbase_t + ch * 32, r);
           tmem_ld_wait();
+          if (full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int k = key0 + ch * 32 + e;
-            const float v = (full || (k >= key_lo && k < key_hi)) ? u2f(r[e]) : -INFINITY;
-            mloc = fmaxf(mloc, v);
+            for (int e = 0; e < 32; ++e) mq[e & 3] = fmaxf(mq[e & 3], u2f(r[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const bool vis = static_cast<uint32_t>(ch * 32 + e - vlo) < vspan;
+              mq[e & 3] = fmaxf(mq[e & 3], vis ? u2f(r[e]) : -INFINITY);
+            }
           }
         }
+        const float mloc = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         M.xchg[j & 1][L] = mloc;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&M.xchg_bar));
@@ -266,21 +276,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l *= fac;
         // the P buffer is free once the previous tile's P.V has completed
         if (j > 0 && !(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
+        float lq[2] = {0.f, 0.f};
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t r[32];
           tmem_ld32(sbase_t + ch * 32, r);
           tmem_ld_wait();
           float pv[32];
+          if (full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int k = key0 + ch * 32 + e;
-            const bool vis = full || (k >= key_lo && k < key_hi);
-            pv[e] = vis ? ex2(fmaf(u2f(r[e]), cl2, -m_new)) : 0.f;
-            l += pv[e];
+            for (int e = 0; e < 32; ++e) pv[e] = ex2(fmaf(u2f(r[e]), cl2, -m_new));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const bool vis = static_cast<uint32_t>(ch * 32 + e - vlo) < vspan;
+              pv[e] = vis ? ex2(fmaf(u2f(r[e]), cl2, -m_new)) : 0.f;
+            }
           }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) lq[e & 1] += pv[e];
           store_p_chunk<E4M3>(smem + C::kOffP, row, half, ch, pv);
         }
+        l += lq[0] + lq[1];
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
