@@ -6,13 +6,21 @@
 //   S[128 heads x 256 keys]  = Q[128 x 576] . [c | kpe]^T      (QK^T, K = 576)
 //   O[128 heads x 512 dims] += P[128 x 256] . c[256 x 512]      (V is c itself)
 // with S (two stages) and O in tensor memory.  Roles (12 warps per CTA):
-//   warps 0-3  softmax: online max / exp2 / row sums, P (bf16 or e4m3) to smem
+//   warps 0-3  softmax: online max / exp2 / row sums, P (bf16 or e4m3) into
+//              tensor memory over the S it came from (below)
 //   warps 4-7  correction: rescale O when the row max moves, final epilogue
 //   warp 8     MMA issue (leader CTA, one thread) and TMEM allocation
 //   warp 9     TMA loads of Q (once per piece of work)
 //   warp 10    TMA loads of K blocks and V pages into one ring of 16 KB slots,
 //              in exactly the order the MMAs consume them, page ids read a tile ahead
 //   warp 11    idle
+// P.V takes P as an A operand in tensor memory, where lane half h of a CTA reads
+// its rows from its own lanes: S leaves keys [0, 128) of a row in the lower half
+// and keys [128, 256) in the upper half, so each softmax thread writes its own
+// keys of P over S columns it has already read, the two halves swap theirs
+// through a small shared buffer, and both halves end with the whole row.  P thus
+// lives in the S stage of its tile: two tiles' P in flight, no shared-memory P
+// buffer held until P.V completes, and no shared-memory reads of A in P.V.
 // The split follows the batch schedule (schedule.cuh); a row owned by one
 // cluster is written to the output, other pieces to workspace partials that
 // the reduction kernel combines.  Every mbarrier wait is bounded: on timeout
@@ -31,6 +39,7 @@
 namespace mla {
 namespace tc {
 
+
 constexpr int kThreads = 384;
 constexpr int kMaxSegs = 256;
 // Rescale O only when a row's max grows by more than 2^8: P stays <= 256
@@ -44,7 +53,11 @@ struct Cfg {
   static constexpr int kNKb = kNLat + 1;         // QK^T contraction blocks (latent + rope)
   static constexpr int kRopeSteps = E4M3 ? 2 : 4;
   static constexpr uint32_t kQBytes = kNLat * 8192 + (E4M3 ? 4096 : 8192);
-  static constexpr int kPBytes = E4M3 ? 16384 : 32768;
+  // P of one row-half of 128 keys: 32-bit words, and the bytes of its exchange row
+  static constexpr int kPWords = E4M3 ? 32 : 64;
+  static constexpr int kXRow = 4 * kPWords;
+  static constexpr int kXBytes = 2 * 64 * kXRow;  // [half][row] exchange rows
+  static constexpr int kPCols = E4M3 ? 64 : 128;  // TMEM columns of a full P row
   // One ring of 16 KB slots holds, in consumption order, the K blocks of a tile (one
   // slot each: this CTA's 128 keys x 128 B) and its V pages (this CTA's columns of 64
   // keys: two slots in bf16, one per output chunk; one slot in e4m3).
@@ -55,8 +68,8 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 0);
   static constexpr uint32_t kIdescPV = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 1);
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + kNKb * 8192;
-  static constexpr int kOffRing = kOffP + kPBytes;
+  static constexpr int kOffX = kOffQ + kNKb * 8192;
+  static constexpr int kOffRing = kOffX + kXBytes;
   static constexpr int kOffSeg = kOffRing + kNS * kSlot;
   static constexpr int kOffMisc = kOffSeg + kMaxSegs * (int)sizeof(Segment);
 };
@@ -65,13 +78,17 @@ struct Misc {
   uint64_t q_full, q_empty;
   uint64_t full[10], empty[10];  // ring slots
   uint64_t s_full[2];
-  uint64_t pv_ready;    // leader: one arrival per CTA, P written and O corrected for the next P.V
-  uint64_t pv_local;    // this CTA's 4 softmax + 4 correction warps, forwarded to the leader's pv_ready
-  uint64_t tail_ready;  // leader: the peer zeroed the tail of a request's last page
-  uint64_t o_done, cor_ready, tail_bar, xchg_bar;
+  // the per-tile barriers come in pairs indexed by tile parity: the softmax may run one
+  // tile ahead of the correction and of the P.V, never two
+  uint64_t pv_ready[2];   // leader: one arrival per CTA, P written and O corrected for the next P.V
+  uint64_t pv_local[2];   // this CTA's 4 softmax + 4 correction warps, forwarded to the leader's pv_ready
+  uint64_t tail_ready;    // leader: the peer zeroed the tail of a request's last page
+  uint64_t o_done[2];     // P.V of a tile complete
+  uint64_t cor_ready[2];  // softmax -> correction: the tile's rescale factor is posted
+  uint64_t tail_bar, xchg_bar;
   float xchg[2][128];             // per-tile row-max exchange between the two halves of a row
   float xsum[128];                // final row-sum exchange
-  float corr[128];                // per-tile rescale factor, softmax -> correction
+  float corr[2][128];             // per-tile rescale factor, softmax -> correction
   float fin_l[2][128], fin_m[2][128];  // final row statistics, double-buffered by segment
   uint32_t tmem_base;
   uint32_t err;
@@ -112,37 +129,32 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 32 probabilities to bf16 pairs (16 words) or e4m3 quadruples (8 words), key order
 template <bool E4M3>
-__device__ __forceinline__ void store_p_chunk(uint8_t* sP, int row, int half, int ch, const float (&p)[32]) {
+__device__ __forceinline__ void pack_p(const float (&p)[32], uint32_t (&w)[E4M3 ? 8 : 16]) {
   if constexpr (!E4M3) {
-    // keys [128 half + 32 ch, +32) of the row: P block 2 half + ch/2, bytes 64 (ch & 1) .. +64
-    uint8_t* blk = sP + (2 * half + (ch >> 1)) * 8192;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(p[8 * q + 2 * e], p[8 * q + 2 * e + 1]);
-        w[e] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      *reinterpret_cast<uint4*>(blk + sw128_offset(row, 4 * (ch & 1) + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int e = 0; e < 16; ++e) {
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(p[2 * e], p[2 * e + 1]);
+      w[e] = *reinterpret_cast<uint32_t*>(&h2);
     }
   } else {
-    // keys [128 half + 32 ch, +32): P block `half`, bytes 32 ch .. +32
-    uint8_t* blk = sP + half * 8192;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i0 = 16 * q + 4 * e;
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[i0], p[i0 + 1]), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[i0 + 2], p[i0 + 3]), __NV_SATFINITE, __NV_E4M3);
-        w[e] = lo | (hi << 16);
-      }
-      *reinterpret_cast<uint4*>(blk + sw128_offset(row, 2 * ch + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[4 * e], p[4 * e + 1]), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[4 * e + 2], p[4 * e + 3]), __NV_SATFINITE, __NV_E4M3);
+      w[e] = lo | (hi << 16);
     }
   }
+}
+
+// Order in which a thread turns its four 32-key chunks of S into P.  P chunk c of
+// half h lands in columns (kPCols / 2) h + (kPCols / 8) c; each order writes only
+// columns of S chunks the thread has already read (S chunk c: columns 32 c .. +32).
+template <bool E4M3>
+__device__ __forceinline__ int chunk_order(int half, int k) {
+  if (half == 0) return k;
+  return E4M3 ? (k < 2 ? 1 - k : k) : 3 - k;
 }
 
 template <bool E4M3>
@@ -155,7 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   Misc& M = *reinterpret_cast<Misc*>(smem + C::kOffMisc);
   Segment* segs = reinterpret_cast<Segment*>(smem + C::kOffSeg);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t sQ = sbase + C::kOffQ, sP = sbase + C::kOffP, sRing = sbase + C::kOffRing;
+  const uint32_t sQ = sbase + C::kOffQ, sRing = sbase + C::kOffRing;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const int cl = blockIdx.x >> 1;
@@ -182,12 +194,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&M.s_full[i]), 1);
+      mbar_init(smem_addr(&M.pv_ready[i]), 2);
+      mbar_init(smem_addr(&M.pv_local[i]), 8);
+      mbar_init(smem_addr(&M.o_done[i]), 1);
+      mbar_init(smem_addr(&M.cor_ready[i]), 4);
     }
-    mbar_init(smem_addr(&M.pv_ready), 2);
-    mbar_init(smem_addr(&M.pv_local), 8);
     mbar_init(smem_addr(&M.tail_ready), 1);
-    mbar_init(smem_addr(&M.o_done), 1);
-    mbar_init(smem_addr(&M.cor_ready), 4);
     mbar_init(smem_addr(&M.tail_bar), 1);
     mbar_init(smem_addr(&M.xchg_bar), 4);
     fence_mbar_init();
@@ -274,11 +286,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fac = 1.f;
         }
         l *= fac;
-        // the P buffer is free once the previous tile's P.V has completed
-        if (j > 0 && !(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
+        // P of this tile overwrites its S stage, which this tile's QK^T (complete at s_full)
+        // wrote after the P.V of tile j - 2 had read the stage's previous P
+        const uint32_t pcol = tmem + lanebase + st * 128;
+        uint8_t* xrow = smem + C::kOffX + (half * 64 + row) * C::kXRow;
+        const int xsw = row & 7;  // 16-byte units of an exchange row, XOR-swizzled by row
         float lq[2] = {0.f, 0.f};
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int k = 0; k < 4; ++k) {
+          const int ch = chunk_order<E4M3>(half, k);
           uint32_t r[32];
           tmem_ld32(sbase_t + ch * 32, r);
           tmem_ld_wait();
@@ -295,14 +311,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int e = 0; e < 32; ++e) lq[e & 1] += pv[e];
-          store_p_chunk<E4M3>(smem + C::kOffP, row, half, ch, pv);
+          constexpr int kW = E4M3 ? 8 : 16;
+          uint32_t w[kW];
+          pack_p<E4M3>(pv, w);
+          if constexpr (E4M3) tmem_st8(pcol + (C::kPCols / 2) * half + (C::kPCols / 8) * ch, w);
+          else tmem_st16(pcol + (C::kPCols / 2) * half + (C::kPCols / 8) * ch, w);
+#pragma unroll
+          for (int q = 0; q < kW / 4; ++q) {
+            const int u = ch * (kW / 4) + q;
+            *reinterpret_cast<uint4*>(xrow + 16 * (u ^ xsw)) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
         }
         l += lq[0] + lq[1];
-        tc_fence_before();
-        fence_proxy_async_smem();
+        // swap halves: this thread's row gets the other half's 128 keys of P
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&M.pv_local));
-        M.corr[L] = fac;
+        if (lane == 0) mbar_arrive(smem_addr(&M.xchg_bar));
+        if (!(ok = kwait(M, smem_addr(&M.xchg_bar), xph & 1))) break;
+        ++xph;
+        {
+          const uint8_t* xo = smem + C::kOffX + ((half ^ 1) * 64 + row) * C::kXRow;
+#pragma unroll 1
+          for (int b = 0; b < C::kPWords / 32; ++b) {
+            uint32_t w[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 v = *reinterpret_cast<const uint4*>(xo + 16 * ((8 * b + q) ^ xsw));
+              w[4 * q] = v.x;
+              w[4 * q + 1] = v.y;
+              w[4 * q + 2] = v.z;
+              w[4 * q + 3] = v.w;
+            }
+            tmem_st32(pcol + (C::kPCols / 2) * (half ^ 1) + 32 * b, w);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&M.pv_local[st]));
+        M.corr[st][L] = fac;
         if (i == n - 1) {
           // final row statistics: the two halves of the row add their sums
           M.xsum[L] = l;
@@ -314,7 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           M.fin_m[s & 1][L] = m_new;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&M.cor_ready));
+        if (lane == 0) mbar_arrive(smem_addr(&M.cor_ready[st]));
         m_ref = m_new;
       }
     }
@@ -331,10 +377,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Segment sg = segs[s];
       const int n = sg.tile_end - sg.tile_begin;
       for (int i = 0; i < n; ++i, ++j) {
-        if (!(ok = kwait(M, smem_addr(&M.cor_ready), j & 1))) break;
-        const float fac = M.corr[L];
+        const int st = j & 1;
+        if (!(ok = kwait(M, smem_addr(&M.cor_ready[st]), (j >> 1) & 1))) break;
+        const float fac = M.corr[st][L];
         if (i > 0 && __any_sync(0xffffffffu, fac != 1.f)) {
-          if (!(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
+          // O holds tiles < j once the P.V of tile j - 1 completes
+          if (!(ok = kwait(M, smem_addr(&M.o_done[st ^ 1]), ((j - 1) >> 1) & 1))) break;
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
@@ -349,17 +397,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&M.pv_local));
+        if (lane == 0) mbar_arrive(smem_addr(&M.pv_local[st]));
         if (warp == 4) {
           // forward this CTA's readiness to the leader: one cross-CTA arrive per tile
-          if (!(ok = kwait(M, smem_addr(&M.pv_local), j & 1))) break;
-          if (lane == 0) mbar_arrive_cluster(lead(M.pv_ready));
+          if (!(ok = kwait(M, smem_addr(&M.pv_local[st]), (j >> 1) & 1))) break;
+          if (lane == 0) mbar_arrive_cluster(lead(M.pv_ready[st]));
           __syncwarp();
         }
       }
       if (!ok) break;
       // epilogue: O / l to the output (whole row) or to the workspace partial
-      if (!(ok = kwait(M, smem_addr(&M.o_done), (j - 1) & 1))) break;
+      if (!(ok = kwait(M, smem_addr(&M.o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1))) break;
       tc_fence_after();
       const float lrow = M.fin_l[s & 1][L], mrow = M.fin_m[s & 1][L];
       // P.V ran on the stored codes of c: the value scale (the key cache's descale) applies here
@@ -430,8 +478,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return true;
       };
       auto qk = [&](int jt) -> bool {
-        // S stage jt & 1 was last read by the softmax of tile jt - 2, whose P.V was
-        // issued (after its pv_ready) before this QK^T: no separate wait
+        // S stage jt & 1 was last read by the softmax of tile jt - 2 and, as its P, by that
+        // tile's P.V, issued after its pv_ready and before this QK^T; the tensor pipe runs
+        // MMAs in issue order: no separate wait
         const int st = jt & 1;
         const uint32_t d = tmem + st * 128;
 #pragma unroll 1
@@ -460,7 +509,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return true;
       };
       auto pv = [&](bool first, int tile) -> bool {
-        if (!kwait(M, smem_addr(&M.pv_ready), pvc & 1)) return false;
+        const int pst = pvc & 1;
+        if (!kwait(M, smem_addr(&M.pv_ready[pst]), (pvc >> 1) & 1)) return false;
         tc_fence_after();
 #pragma unroll 1
         for (int vp = 0; vp < 4; ++vp) {
@@ -476,18 +526,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           for (int t = 0; t < C::kPvSteps; ++t) {
-            const uint32_t pa = E4M3 ? sP + (vp >> 1) * 8192 + 64 * (vp & 1) + 32 * t : sP + vp * 8192 + 32 * t;
-            const uint64_t ad = smem_desc_sw128(pa, 16, 1024);
+            const uint32_t acc = (first && vp == 0 && t == 0) ? 0u : 1u;
+            // keys [64 vp + (32 or 16) t, ...) of P: 8 columns of stage pst per step
+            const uint32_t a_tm = tmem + pst * 128 + (C::kPCols / 4) * vp + 8 * t;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               const uint32_t vb = E4M3 ? va[0] + c * 8192 + t * 4096 : va[c] + t * 2048;
-              const uint64_t bd = smem_desc_sw128(vb, 8192, 1024);
-              mma_ss<2, KIND>(tmem + 256 + 128 * c, ad, bd, C::kIdescPV, (first && vp == 0 && t == 0) ? 0u : 1u);
+              mma_ts<2, KIND>(tmem + 256 + 128 * c, a_tm, smem_desc_sw128(vb, 8192, 1024), C::kIdescPV, acc);
             }
           }
           for (int it = 0; it < C::kVItems; ++it) mma_commit_pair(smem_addr(&M.empty[slot[it]]), 0x3);
         }
-        mma_commit_pair(smem_addr(&M.o_done), 0x3);
+        mma_commit_pair(smem_addr(&M.o_done[pst]), 0x3);
         ++pvc;
         return true;
       };
