@@ -15,23 +15,24 @@
 
 namespace mla {
 
-// ------------------------------------------------------------------ reduction
-// grid (ceil(H / 4), R), block 128: each warp combines one head of one row,
-// each lane 16 consecutive dims (four float4 loads per piece).
-__global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p) {
-  const int r = blockIdx.y;
-  const int h = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (h >= p.H) return;
+// One CTA per (row, 64 dims): the row's pieces combined with weights
+// exp2(lse_i - lse), lse = log2 of the summed exp2(lse_i) (one piece: weight 1, a
+// copy).  Pieces are workspace slots laid out [dim / 4][head][dim % 4], so a
+// warp's float4 loads are 512 contiguous bytes; the block transposes through
+// shared memory and writes the output head-major with each head's dims contiguous.
+constexpr int kReduceDims = 64;
+
+__global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
+  __shared__ float tile[kHeadsPad][kReduceDims + 1];  // [head][dim], padded against bank conflicts
+  const int r = blockIdx.y, d0 = blockIdx.x * kReduceDims;
+  const int h = threadIdx.x & (kHeadsPad - 1), dg = threadIdx.x >> 7;  // 32 dims per thread
   const WsLayout L = ws_layout(p.B * p.Sq, p.num_clusters);
   const RowInfo ri = reinterpret_cast<const RowInfo*>(p.ws + L.row_info)[r];
-  if (ri.n_parts == 1) return;  // the split-KV kernel wrote this row directly
-  const size_t out_row = (size_t)r * p.H + h;
-  float acc[16];
+  float acc[32];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
   float lse2 = -INFINITY;
-  if (ri.n_parts > 1) {
+  if (h < p.H && ri.n_parts > 0) {
     const float* plse = reinterpret_cast<const float*>(p.ws + L.partial_lse);
     const float* po = reinterpret_cast<const float*>(p.ws + L.partial_o);
     float mx = -INFINITY;
@@ -45,38 +46,51 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p) {
         const size_t slot = (size_t)(ri.first_slot + i);
         const float li = plse[slot * kHeadsPad + h];
         if (li == -INFINITY) continue;  // an empty piece adds nothing (and its partial is never read)
-        const float w = exp2f(li - lse2);
-        const float4* src = reinterpret_cast<const float4*>(po + (slot * kHeadsPad + h) * kDLatent) + lane * 4;
+        const float w = ri.n_parts == 1 ? 1.f : exp2f(li - lse2);
+        const float4* src = reinterpret_cast<const float4*>(po) + (slot * (kDLatent / 4) + (d0 + 32 * dg) / 4) * kHeadsPad + h;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const float4 x = __ldcs(src + v);
-          acc[4 * v + 0] += w * x.x;
-          acc[4 * v + 1] += w * x.y;
-          acc[4 * v + 2] += w * x.z;
-          acc[4 * v + 3] += w * x.w;
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = __ldcs(src + (size_t)q * kHeadsPad);
+          acc[4 * q] += w * x.x;
+          acc[4 * q + 1] += w * x.y;
+          acc[4 * q + 2] += w * x.z;
+          acc[4 * q + 3] += w * x.w;
         }
       }
     }
   }
   // n_parts == 0: no visible key, O = 0 and LSE = -inf
-  if (p.out_f32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row * kDLatent) + lane * 4;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
-  } else {
-    __nv_bfloat162 b2[8];
+  for (int e = 0; e < 32; ++e) tile[h][32 * dg + e] = acc[e];
+  __syncthreads();
+  const int hh = threadIdx.x >> 1, part = threadIdx.x & 1;  // one head's 32 dims per thread
+  if (hh < p.H) {
+    const size_t out_row = (size_t)r * p.H + hh;
+    const float* t = &tile[hh][32 * part];
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row * kDLatent + d0 + 32 * part);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) b2[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + out_row * kDLatent) + lane * 2;
-    dst[0] = *reinterpret_cast<uint4*>(&b2[0]);
-    dst[1] = *reinterpret_cast<uint4*>(&b2[4]);
+      for (int v = 0; v < 8; ++v) dst[v] = make_float4(t[4 * v], t[4 * v + 1], t[4 * v + 2], t[4 * v + 3]);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + out_row * kDLatent + d0 + 32 * part);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(t[8 * v + 2 * e], t[8 * v + 2 * e + 1]);
+          w[e] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
   }
-  if (p.lse && lane == 0) p.lse[out_row] = lse2 * 0.69314718055994530942f;
+  if (p.lse && blockIdx.x == 0 && dg == 0 && h < p.H) p.lse[(size_t)r * p.H + h] = lse2 * 0.69314718055994530942f;
 }
 
 cudaError_t launch_reduce(const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid((p.H + 3) / 4, p.B * p.Sq);
-  reduce_kernel<<<grid, 128, 0, stream>>>(p);
+  dim3 grid(kDLatent / kReduceDims, p.B * p.Sq);
+  reduce_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -21,9 +21,8 @@
 // through a small shared buffer, and both halves end with the whole row.  P thus
 // lives in the S stage of its tile: two tiles' P in flight, no shared-memory P
 // buffer held until P.V completes, and no shared-memory reads of A in P.V.
-// The split follows the batch schedule (schedule.cuh); a row owned by one
-// cluster is written to the output, other pieces to workspace partials that
-// the reduction kernel combines.  Every mbarrier wait is bounded: on timeout
+// The split follows the batch schedule (schedule.cuh); every piece of a row
+// goes to a workspace slot that the reduction kernel turns into the output.  Every mbarrier wait is bounded: on timeout
 // the kernel records kErrTimeout, unwinds its roles, lets in-flight copies
 // land and frees TMEM.
 #include <cuda_bf16.h>
@@ -53,16 +52,18 @@ struct Cfg {
   static constexpr int kNKb = kNLat + 1;         // QK^T contraction blocks (latent + rope)
   static constexpr int kRopeSteps = E4M3 ? 2 : 4;
   static constexpr uint32_t kQBytes = kNLat * 8192 + (E4M3 ? 4096 : 8192);
-  // P of one row-half of 128 keys: 32-bit words, and the bytes of its exchange row
+  // P of one row-half of 128 keys in 32-bit words.  The halves swap P through an
+  // exchange buffer of [row][half] regions: e4m3 in one round (128 B a region), bf16 in
+  // two rounds of 64 keys (128 B a region), which halves its size.
   static constexpr int kPWords = E4M3 ? 32 : 64;
-  static constexpr int kXRow = 4 * kPWords;
-  static constexpr int kXBytes = 2 * 64 * kXRow;  // [half][row] exchange rows
+  static constexpr int kXRegion = 128;
+  static constexpr int kXBytes = 64 * 2 * kXRegion;
   static constexpr int kPCols = E4M3 ? 64 : 128;  // TMEM columns of a full P row
   // One ring of 16 KB slots holds, in consumption order, the K blocks of a tile (one
   // slot each: this CTA's 128 keys x 128 B) and its V pages (this CTA's columns of 64
   // keys: two slots in bf16, one per output chunk; one slot in e4m3).
   static constexpr int kSlot = 16384;
-  static constexpr int kNS = E4M3 ? 10 : 7;
+  static constexpr int kNS = E4M3 ? 10 : 8;
   static constexpr int kVItems = E4M3 ? 1 : 2;    // ring slots per V page
   static constexpr int kPvSteps = E4M3 ? 2 : 4;  // MMAs per page and output chunk (32 or 16 keys each)
   static constexpr uint32_t kIdescQK = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 0);
@@ -289,9 +290,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // P of this tile overwrites its S stage, which this tile's QK^T (complete at s_full)
         // wrote after the P.V of tile j - 2 had read the stage's previous P
         const uint32_t pcol = tmem + lanebase + st * 128;
-        uint8_t* xrow = smem + C::kOffX + (half * 64 + row) * C::kXRow;
-        const int xsw = row & 7;  // 16-byte units of an exchange row, XOR-swizzled by row
+        // this thread's and its partner's exchange regions (16-byte units XOR-swizzled by row)
+        uint8_t* xmine = smem + C::kOffX + (row * 2 + half) * C::kXRegion;
+        const uint8_t* xpart = smem + C::kOffX + (row * 2 + (half ^ 1)) * C::kXRegion;
+        const int xsw = row & 7;
+        auto xput = [&](int unit, const uint32_t* w4) {
+          *reinterpret_cast<uint4*>(xmine + 16 * (unit ^ xsw)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        };
+        auto xget = [&](int unit, uint32_t* w4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xpart + 16 * (unit ^ xsw));
+          w4[0] = v.x;
+          w4[1] = v.y;
+          w4[2] = v.z;
+          w4[3] = v.w;
+        };
+        auto xbarrier = [&]() -> bool {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&M.xchg_bar));
+          const bool r = kwait(M, smem_addr(&M.xchg_bar), xph & 1);
+          ++xph;
+          return r;
+        };
         float lq[2] = {0.f, 0.f};
+        uint32_t hold0[16], hold1[16];  // bf16: this half's second-round chunks
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           const int ch = chunk_order<E4M3>(half, k);
@@ -314,35 +335,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           constexpr int kW = E4M3 ? 8 : 16;
           uint32_t w[kW];
           pack_p<E4M3>(pv, w);
-          if constexpr (E4M3) tmem_st8(pcol + (C::kPCols / 2) * half + (C::kPCols / 8) * ch, w);
-          else tmem_st16(pcol + (C::kPCols / 2) * half + (C::kPCols / 8) * ch, w);
+          if constexpr (E4M3) {
+            tmem_st8(pcol + (C::kPCols / 2) * half + (C::kPCols / 8) * ch, w);
+            // the region holds this half's 128 keys in key order: chunk ch at units 2 ch, 2 ch + 1
 #pragma unroll
-          for (int q = 0; q < kW / 4; ++q) {
-            const int u = ch * (kW / 4) + q;
-            *reinterpret_cast<uint4*>(xrow + 16 * (u ^ xsw)) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            for (int q = 0; q < 2; ++q) xput(2 * ch + q, w + 4 * q);
+          } else {
+            tmem_st16(pcol + (C::kPCols / 2) * half + (C::kPCols / 8) * ch, w);
+            // first round: this half's chunks k = 0, 1 at units 4 k .. +4; the others wait
+            if (k < 2) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) xput(4 * k + q, w + 4 * q);
+            } else if (k == 2) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) hold0[e] = w[e];
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) hold1[e] = w[e];
+            }
           }
         }
         l += lq[0] + lq[1];
         // swap halves: this thread's row gets the other half's 128 keys of P
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&M.xchg_bar));
-        if (!(ok = kwait(M, smem_addr(&M.xchg_bar), xph & 1))) break;
-        ++xph;
-        {
-          const uint8_t* xo = smem + C::kOffX + ((half ^ 1) * 64 + row) * C::kXRow;
-#pragma unroll 1
-          for (int b = 0; b < C::kPWords / 32; ++b) {
-            uint32_t w[32];
+        if (!(ok = xbarrier())) break;
+        if constexpr (E4M3) {
+          uint32_t w[32];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 v = *reinterpret_cast<const uint4*>(xo + 16 * ((8 * b + q) ^ xsw));
-              w[4 * q] = v.x;
-              w[4 * q + 1] = v.y;
-              w[4 * q + 2] = v.z;
-              w[4 * q + 3] = v.w;
+          for (int q = 0; q < 8; ++q) xget(q, w + 4 * q);
+          tmem_st32(pcol + (C::kPCols / 2) * (half ^ 1), w);
+        } else {
+          const int hp = half ^ 1;
+#pragma unroll 1
+          for (int rd = 0; rd < 2; ++rd) {
+            if (rd == 1) {
+              // the partner has read the first round: this half's second round goes out
+              if (!(ok = xbarrier())) break;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) xput(q, hold0 + 4 * q);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) xput(4 + q, hold1 + 4 * q);
+              if (!(ok = xbarrier())) break;
             }
-            tmem_st32(pcol + (C::kPCols / 2) * (half ^ 1) + 32 * b, w);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              uint32_t w[16];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) xget(4 * c2 + q, w + 4 * q);
+              tmem_st16(pcol + (C::kPCols / 2) * hp + (C::kPCols / 8) * chunk_order<E4M3>(hp, 2 * rd + c2), w);
+            }
           }
+          if (!ok) break;
         }
         tmem_st_wait();
         tc_fence_before();
@@ -406,7 +448,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // epilogue: O / l to the output (whole row) or to the workspace partial
+      // epilogue: O / l and the base-2 log-sum-exp to this piece's workspace slot (the
+      // reduction kernel combines a row's pieces, or copies a whole row, into the output).
+      // Slots are [dim / 4][head][dim % 4]: a warp's float4 store, four dims of 32
+      // consecutive heads, is 512 contiguous bytes.
       if (!(ok = kwait(M, smem_addr(&M.o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1))) break;
       tc_fence_after();
       const float lrow = M.fin_l[s & 1][L], mrow = M.fin_m[s & 1][L];
@@ -414,8 +459,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float inv = p.ckv_descale / lrow;
       const float lse2 = mrow + log2f(lrow);
       const bool live = head < p.H;
-      const size_t orow = (size_t)sg.row * p.H + head;
       const size_t slot = (size_t)sg.row + cl;
+      float4* po = reinterpret_cast<float4*>(p.ws + WL.partial_o) + slot * (kDLatent / 4) * kHeadsPad + head;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t r[32];
@@ -424,43 +469,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // TMEM columns [128 chunk, +128) of this lane hold D columns 256 chunk + 128 half + [0, 128)
         const int d0 = 256 * (c >> 2) + 128 * half + 32 * (c & 3);
         if (live) {
-          if (sg.whole) {
-            if (p.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDLatent + d0);
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv, u2f(r[4 * q + 2]) * inv,
-                                     u2f(r[4 * q + 3]) * inv);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * kDLatent + d0);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  __nv_bfloat162 h2 = __floats2bfloat162_rn(u2f(r[8 * q + 2 * e]) * inv, u2f(r[8 * q + 2 * e + 1]) * inv);
-                  w[e] = *reinterpret_cast<uint32_t*>(&h2);
-                }
-                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.ws + WL.partial_o) +
-                                                    (slot * kHeadsPad + head) * kDLatent + d0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv, u2f(r[4 * q + 2]) * inv,
-                                   u2f(r[4 * q + 3]) * inv);
-          }
+          for (int q = 0; q < 8; ++q)
+            __stcg(po + (size_t)(d0 / 4 + q) * kHeadsPad, make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv,
+                                                                    u2f(r[4 * q + 2]) * inv, u2f(r[4 * q + 3]) * inv));
         }
       }
-      if (live && half == 0) {
-        if (sg.whole) {
-          if (p.lse) p.lse[orow] = lse2 * ln2;
-        } else {
-          reinterpret_cast<float*>(p.ws + WL.partial_lse)[slot * kHeadsPad + head] = lse2;
-        }
-      }
+      if (live && half == 0) reinterpret_cast<float*>(p.ws + WL.partial_lse)[slot * kHeadsPad + head] = lse2;
       tc_fence_before();
     }
   } else if (warp == 8) {

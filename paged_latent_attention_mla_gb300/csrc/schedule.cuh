@@ -7,8 +7,8 @@
 // contiguous shares to G = min(clusters launched, T) clusters of one persistent
 // wave (so every dealing cluster owns at least one tile):
 // cluster c owns global tiles [floor(c*T/G), floor((c+1)*T/G)).
-// The piece of row r owned by cluster c writes partial slot r + c; a row owned
-// by a single cluster is written straight to the output.
+// The piece of row r owned by cluster c writes partial slot r + c, and the
+// reduction kernel turns each row's slots into its output.
 #pragma once
 #include "mla_common.cuh"
 
@@ -20,7 +20,7 @@ struct RowWork {
   int tile_begin;        // first tile (key index / kTileN) of this piece
   int tile_end;          // one past its last tile
   int slot;              // partial slot (r + c)
-  int n_parts;           // 1: this piece is the whole row
+  int n_parts;           // pieces the row is cut into
 };
 
 struct ScheduleView {
@@ -191,7 +191,6 @@ struct Segment {
   int32_t row;
   int32_t tile_begin;
   int32_t tile_end;
-  int32_t whole;  // 1: the row has no other piece (write the output directly)
 };
 
 // Extract cluster c's pieces, in row order, into segs[0..n) (thread 0 of the
@@ -211,7 +210,6 @@ __device__ inline int build_segments(const DecodeParams& p, const ScheduleView& 
     segs[n].row = r;
     segs[n].tile_begin = w.tile_begin;
     segs[n].tile_end = w.tile_end;
-    segs[n].whole = w.n_parts == 1 ? 1 : 0;
     ++n;
   }
   return n;
