@@ -83,7 +83,7 @@ HostPlan plan_rows(const int32_t* seq_lens, int B, int Sq, int causal, int windo
     visible_range(K, Sq, r % Sq, causal, window_left, lo, hi);
     tile_span(lo, hi, tlo, nt);
     n[r] = nt;
-    prefix[r + 1] = prefix[r] + nt;
+    prefix[r + 1] = prefix[r] + (nt > 0 ? nt + kPieceCost : 0);
   }
   const long long T = prefix[hp.R];
   hp.T = (int)T;
@@ -92,7 +92,8 @@ HostPlan plan_rows(const int32_t* seq_lens, int B, int Sq, int causal, int windo
   std::vector<int> segs(G, 0);
   for (int r = 0; r < hp.R; ++r) {
     if (n[r] == 0) continue;
-    const int cf = cluster_of_tile(prefix[r], T, G), cl = cluster_of_tile(prefix[r] + n[r] - 1, T, G);
+    const long long pb = prefix[r] + kPieceCost;
+    const int cf = cluster_of_tile(pb, T, G), cl = cluster_of_tile(pb + n[r] - 1, T, G);
     if (cl - cf + 1 > hp.max_parts) hp.max_parts = cl - cf + 1;
     for (int c = cf; c <= cl; ++c) segs[c]++;
   }

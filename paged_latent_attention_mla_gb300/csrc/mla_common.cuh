@@ -17,6 +17,10 @@ constexpr int kRowsPerCta = 64;
 constexpr int kHeadsPad = 2 * kRowsPerCta;  // one M=128 tile of heads per (request, token) row
 constexpr int kMaxHeads = kHeadsPad;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded device waits give up after 2 s
+// The batch deal charges every row with visible keys this many virtual tiles ahead of its
+// real ones: what starting a piece costs a cluster (its Q, the pipeline refill, the
+// epilogue), so that a cluster dealt many short rows gets fewer tiles.
+constexpr int kPieceCost = 1;
 
 // status bits each CTA of the split-KV kernel leaves in its own status word
 constexpr uint32_t kErrTimeout = 1u;
@@ -38,7 +42,7 @@ struct WsHeader {
 struct RowInfo {
   int32_t tile_lo;     // first KV tile (key index / kTileN) holding a visible key
   int32_t n_tiles;     // tiles from tile_lo on that hold visible keys (0: empty row)
-  int32_t prefix;      // tiles of all earlier rows, laid end to end
+  int32_t prefix;      // virtual tiles of all earlier rows (the batch deal's row start)
   int32_t first_slot;  // partial slot of the row's first piece
   int32_t n_parts;     // pieces the row is cut into (0: empty, 1: written directly)
   int32_t key_lo;      // visible keys [key_lo, key_hi)
@@ -94,7 +98,7 @@ __host__ __device__ inline void tile_span(int lo, int hi, int& tile_lo, int& n_t
   n_tiles = (hi + kTileN - 1) / kTileN - tile_lo;
 }
 
-// cluster holding global tile x when T tiles are dealt to G clusters in equal
+// cluster holding virtual tile x when T virtual tiles are dealt to G clusters in equal
 // contiguous shares [floor(c*T/G), floor((c+1)*T/G))
 __host__ __device__ inline int cluster_of_tile(long long x, long long T, long long G) {
   return (int)(((x + 1) * G - 1) / T);

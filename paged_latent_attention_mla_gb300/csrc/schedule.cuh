@@ -2,11 +2,13 @@
 // split-KV kernel (in scratch shared memory, before the tile buffers are used).
 //
 // Every (request, token) row r = b * Sq + t has visible keys [lo, hi) and the
-// KV tiles [tile_lo, tile_lo + n_r) that hold them.  The tiles of all rows are
-// laid end to end (row r's start is the prefix sum P_r) and dealt out in equal
-// contiguous shares to G = min(clusters launched, T) clusters of one persistent
-// wave (so every dealing cluster owns at least one tile):
-// cluster c owns global tiles [floor(c*T/G), floor((c+1)*T/G)).
+// KV tiles [tile_lo, tile_lo + n_r) that hold them.  Each row with n_r > 0 costs
+// n_r + kPieceCost virtual tiles: kPieceCost for starting a piece, then its real
+// tiles.  The rows' virtual tiles are laid end to end (row r starts at the prefix
+// sum P_r, its real tiles at P_r + kPieceCost) and dealt out in equal contiguous
+// shares to G = min(clusters launched, T) clusters of one persistent wave:
+// cluster c owns virtual tiles [floor(c*T/G), floor((c+1)*T/G)) and works on the
+// real tiles among them.
 // The piece of row r owned by cluster c writes partial slot r + c, and the
 // reduction kernel turns each row's slots into its output.
 #pragma once
@@ -61,8 +63,9 @@ __device__ inline ScheduleView build_schedule(const DecodeParams& p, int32_t* sc
   for (int r = r0; r < r1; ++r) {
     int lo, hi, tlo, n;
     row_span(p, r, clamp_len(p, r / p.Sq, err_flag), lo, hi, tlo, n);
-    prefix[r] = n;
-    local += n;
+    const int cost = n > 0 ? n + kPieceCost : 0;
+    prefix[r] = cost;
+    local += cost;
   }
   // inclusive scan of per-thread sums: warp scans, then a scan of warp totals
   const int lane = tid & 31, warp = tid >> 5;
@@ -102,7 +105,7 @@ __device__ inline ScheduleView build_schedule(const DecodeParams& p, int32_t* sc
   return s;
 }
 
-// largest row r with prefix[r] <= x (x < T): the row holding global tile x
+// largest row r with prefix[r] <= x (x < T): the row holding virtual tile x
 __device__ inline int row_of_tile(const ScheduleView& s, int x) {
   int lo = 0, hi = s.R - 1;
   while (lo < hi) {
@@ -124,12 +127,13 @@ __device__ inline void cluster_rows(const ScheduleView& s, int c, int& first, in
   last = row_of_tile(s, (int)(e - 1));
 }
 
-// the piece of row r that cluster c owns (call for r in cluster_rows(c))
+// the piece of row r that cluster c owns (call for r in cluster_rows(c)): the row's
+// real tiles inside the cluster's share, if any
 __device__ inline bool row_piece(const DecodeParams& p, const ScheduleView& s, int c, int r, RowWork& w) {
-  const int n = s.prefix[r + 1] - s.prefix[r];
+  const int n = s.prefix[r + 1] - s.prefix[r] - kPieceCost;
   if (n <= 0) return false;
   const long long cb = cluster_tile_begin(c, s.T, s.G), ce = cluster_tile_begin(c + 1, s.T, s.G);
-  const long long pb = s.prefix[r], pe = s.prefix[r] + n;
+  const long long pb = s.prefix[r] + kPieceCost, pe = pb + n;
   const long long gb = pb > cb ? pb : cb, ge = pe < ce ? pe : ce;
   if (gb >= ge) return false;
   int lo, hi, tlo, nn;
@@ -163,8 +167,9 @@ __device__ inline void write_row_table(const DecodeParams& p, const ScheduleView
     ri.key_hi = hi;
     ri.pad = 0;
     if (n > 0) {
-      const int c_first = cluster_of_tile(s.prefix[r], s.T, s.G);
-      const int c_last = cluster_of_tile((long long)s.prefix[r] + n - 1, s.T, s.G);
+      const long long pb = (long long)s.prefix[r] + kPieceCost;
+      const int c_first = cluster_of_tile(pb, s.T, s.G);
+      const int c_last = cluster_of_tile(pb + n - 1, s.T, s.G);
       ri.first_slot = r + c_first;
       ri.n_parts = c_last - c_first + 1;
     } else {

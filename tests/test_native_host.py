@@ -49,9 +49,10 @@ def cfg(**kw):
     return n.make_config(**base)
 
 
-def host_plan(lens, Sq, causal, window, G, tile=256):
-    """Independent restatement of the batch deal: the rows' visible tiles end to end, dealt in equal
-    contiguous shares to min(G, T) clusters; a row's pieces are the clusters whose share meets it."""
+def host_plan(lens, Sq, causal, window, G, tile=256, piece_cost=1):
+    """Independent restatement of the batch deal: each row with visible keys costs piece_cost virtual
+    tiles followed by its real tiles; the rows' virtual tiles end to end are dealt in equal contiguous
+    shares to min(G, T) clusters; a row's pieces are the clusters whose share meets its real tiles."""
     rows = []
     for K in lens:
         for t in range(Sq):
@@ -60,14 +61,16 @@ def host_plan(lens, Sq, causal, window, G, tile=256):
             hi, lo = min(max(hi, 0), K), min(max(lo, 0), K)
             lo = min(lo, hi)
             rows.append(0 if hi <= lo else (hi + tile - 1) // tile - lo // tile)
-    T = sum(rows)
+    cost = [nt + piece_cost if nt else 0 for nt in rows]
+    T = sum(cost)
     Ge = max(1, min(G, T))
     shares = [(c * T // Ge, (c + 1) * T // Ge) for c in range(Ge)]
     assert all(e > b for b, e in shares) or T == 0
     parts, start = [], 0
-    for nt in rows:
-        parts.append(sum(1 for b, e in shares if b < start + nt and start < e) if nt else 0)
-        start += nt
+    for nt, ct in zip(rows, cost):
+        lo, hi = start + piece_cost, start + piece_cost + nt
+        parts.append(sum(1 for b, e in shares if b < hi and lo < e) if nt else 0)
+        start += ct
     return len(rows), max([1] + parts)
 
 
