@@ -33,28 +33,44 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
   for (int i = 0; i < 32; ++i) acc[i] = 0.f;
   float lse2 = -INFINITY;
   if (h < p.H && ri.n_parts > 0) {
-    const float* plse = reinterpret_cast<const float*>(p.ws + L.partial_lse);
-    const float* po = reinterpret_cast<const float*>(p.ws + L.partial_o);
+    const float* plse = reinterpret_cast<const float*>(p.ws + L.partial_lse) + (size_t)ri.first_slot * kHeadsPad + h;
+    const float4* po = reinterpret_cast<const float4*>(p.ws + L.partial_o) +
+                       ((size_t)ri.first_slot * (kDLatent / 4) + (d0 + 32 * dg) / 4) * kHeadsPad + h;
+    const int np = ri.n_parts;
+    // the pieces' LSEs: loads issued together, then max and sum
     float mx = -INFINITY;
-    for (int i = 0; i < ri.n_parts; ++i) mx = fmaxf(mx, plse[(size_t)(ri.first_slot + i) * kHeadsPad + h]);
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) mx = fmaxf(mx, plse[(size_t)i * kHeadsPad]);
     const float m0 = mx == -INFINITY ? 0.f : mx;
     float sum = 0.f;
-    for (int i = 0; i < ri.n_parts; ++i) sum += exp2f(plse[(size_t)(ri.first_slot + i) * kHeadsPad + h] - m0);
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) sum += exp2f(plse[(size_t)i * kHeadsPad] - m0);
     lse2 = sum > 0.f ? m0 + log2f(sum) : -INFINITY;
     if (sum > 0.f) {
-      for (int i = 0; i < ri.n_parts; ++i) {
-        const size_t slot = (size_t)(ri.first_slot + i);
-        const float li = plse[slot * kHeadsPad + h];
-        if (li == -INFINITY) continue;  // an empty piece adds nothing (and its partial is never read)
-        const float w = ri.n_parts == 1 ? 1.f : exp2f(li - lse2);
-        const float4* src = reinterpret_cast<const float4*>(po) + (slot * (kDLatent / 4) + (d0 + 32 * dg) / 4) * kHeadsPad + h;
+      // two pieces per round, their loads issued before any use; an empty piece (LSE -inf,
+      // slot never written) gets weight 0 and is selected away
+      for (int i0 = 0; i0 < np; i0 += 2) {
+        float4 x[2][8];
+        float w[2];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 x = __ldcs(src + (size_t)q * kHeadsPad);
-          acc[4 * q] += w * x.x;
-          acc[4 * q + 1] += w * x.y;
-          acc[4 * q + 2] += w * x.z;
-          acc[4 * q + 3] += w * x.w;
+        for (int u = 0; u < 2; ++u) {
+          const int i = i0 + u < np ? i0 + u : i0;
+          const float li = plse[(size_t)i * kHeadsPad];
+          w[u] = (i0 + u < np && li != -INFINITY) ? exp2f(li - lse2) : 0.f;
+          const float4* src = po + (size_t)i * (kDLatent / 4) * kHeadsPad;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[u][q] = __ldcs(src + (size_t)q * kHeadsPad);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (w[u] == 0.f) continue;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            acc[4 * q] += w[u] * x[u][q].x;
+            acc[4 * q + 1] += w[u] * x[u][q].y;
+            acc[4 * q + 2] += w[u] * x[u][q].z;
+            acc[4 * q + 3] += w[u] * x[u][q].w;
+          }
         }
       }
     }
