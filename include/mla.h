@@ -75,6 +75,10 @@ typedef enum { MLA_BF16 = 0, MLA_E4M3 = 1, MLA_F32 = 2 } mla_dtype_t;
  *                     (MLA_ERR_UNSUPPORTED otherwise): one scale for the key cache.
  *  num_clusters       0: one persistent wave sized from the device (default);
  *                     >0: use this many 2-CTA clusters (testing and partitioning)
+ *  split_timing       optional pair of cudaEvent_t handles (caller-owned, already
+ *                     created): when both are non-NULL, mla_decode records [0] just
+ *                     before and [1] just after the split-KV kernel on the call's
+ *                     stream, so the kernel can be timed alone; NULL: nothing recorded
  */
 typedef struct {
   int seq_len_q;
@@ -87,6 +91,7 @@ typedef struct {
   float ckv_descale;
   float kpe_descale;
   int num_clusters;
+  void* split_timing[2];
 } mla_config_t;
 
 /*

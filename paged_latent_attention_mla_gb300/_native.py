@@ -42,6 +42,7 @@ class MlaConfig(ctypes.Structure):
         ("ckv_descale", ctypes.c_float),
         ("kpe_descale", ctypes.c_float),
         ("num_clusters", ctypes.c_int),
+        ("split_timing", ctypes.c_void_p * 2),
     ]
 
 

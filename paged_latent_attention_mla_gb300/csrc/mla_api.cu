@@ -230,8 +230,13 @@ mla_status_t mla_decode(const void* q_latent, const void* q_rope, const void* ck
 
   KvMaps maps;
   if (!encode_kv_maps(&maps, ckv_cache, kpe_cache, q_latent, q_rope, e4m3, cfg->num_pages, R, H)) return MLA_ERR_CUDA;
+  const bool timed = cfg->split_timing[0] && cfg->split_timing[1];
+  if (timed && cudaEventRecord(static_cast<cudaEvent_t>(cfg->split_timing[0]), stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
   cudaError_t e = launch_split_kv(p, maps, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
+  if (timed && cudaEventRecord(static_cast<cudaEvent_t>(cfg->split_timing[1]), stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
   return cuda_status(launch_reduce(p, stream));
 }
 
