@@ -183,6 +183,18 @@ MLA_API mla_status_t mla_debug_mask(const int32_t *seq_lens, int B, int window_l
                             uint32_t *bits, cudaStream_t stream);
 
 /*
+ * Debug check of the bounded device waits: launches one 2-CTA cluster that allocates
+ * tensor memory and waits on an mbarrier nothing arrives at, giving up after
+ * timeout_us microseconds (1 .. 2000000) the way every wait of the decode kernel
+ * gives up after 2 s: it records a timeout bit, meets its peer, frees the tensor
+ * memory and writes a status word per CTA to status_words (device, 2 x uint32,
+ * caller-owned) instead of hanging or faulting.  Synchronizes the stream and returns
+ * MLA_ERR_TIMEOUT when both words report the timeout, MLA_OK if a wait did not time
+ * out, MLA_ERR_INVALID_ARG for a bad argument.  Not for the decode path.
+ */
+MLA_API mla_status_t mla_debug_wait_timeout(unsigned timeout_us, uint32_t *status_words, cudaStream_t stream);
+
+/*
  * Debug status: synchronizes the stream and reads the status word that the
  * last mla_decode on this workspace left (MLA_OK, or MLA_ERR_TIMEOUT when a
  * bounded device wait gave up).  Not for the decode path.

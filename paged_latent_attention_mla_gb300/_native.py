@@ -20,8 +20,8 @@ MLA_BF16, MLA_E4M3, MLA_F32 = 0, 1, 2
 
 _DTYPES = {torch.bfloat16: MLA_BF16, torch.float8_e4m3fn: MLA_E4M3, torch.float32: MLA_F32}
 
-EXPORTS = ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_debug_gather", "mla_debug_mask", "mla_workspace_status",
-           "mla_status_string")
+EXPORTS = ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_debug_gather", "mla_debug_mask",
+           "mla_debug_wait_timeout", "mla_workspace_status", "mla_status_string")
 
 
 class MlaError(RuntimeError):
@@ -70,11 +70,12 @@ def load(path: str | None = None):
             lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, F, I, P, P, P, I, I, I, cfgp]
             lib.mla_debug_gather.argtypes = [P, P, P, P, I, I, I, cfgp, P, P]
             lib.mla_debug_mask.argtypes = [P, I, I, I, cfgp, P, P]
+            lib.mla_debug_wait_timeout.argtypes = [ctypes.c_uint, P, P]
             lib.mla_workspace_status.argtypes = [P, S, P]
             lib.mla_status_string.argtypes = [I]
             lib.mla_status_string.restype = ctypes.c_char_p
             for fn in ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_debug_gather", "mla_debug_mask",
-                       "mla_workspace_status"):
+                       "mla_debug_wait_timeout", "mla_workspace_status"):
                 getattr(lib, fn).restype = I
             _lib = lib
     return _lib
@@ -149,6 +150,12 @@ def mla_debug_mask(seq_lens, window_left: int, max_k: int, bits, cfg: MlaConfig,
     B = seq_lens.shape[0]
     _check("mla_debug_mask", load().mla_debug_mask(_ptr(seq_lens), int(B), int(window_left), int(max_k),
                                                    ctypes.byref(cfg), _ptr(bits), _stream(stream)))
+
+
+def mla_debug_wait_timeout(timeout_us: int, status_words, stream=None):
+    """Raises MlaError(MLA_ERR_TIMEOUT) when the device wait gave up, as it should."""
+    _check("mla_debug_wait_timeout", load().mla_debug_wait_timeout(ctypes.c_uint(int(timeout_us)), _ptr(status_words),
+                                                                   _stream(stream)))
 
 
 def mla_workspace_status(workspace, stream=None) -> int:

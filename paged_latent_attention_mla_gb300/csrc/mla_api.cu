@@ -264,6 +264,15 @@ mla_status_t mla_debug_mask(const int32_t* seq_lens, int B, int window_left, int
       launch_debug_mask(seq_lens, B, cfg->seq_len_q, cfg->causal ? 1 : 0, window_left, max_k, bits, stream));
 }
 
+mla_status_t mla_debug_wait_timeout(unsigned timeout_us, uint32_t* status_words, cudaStream_t stream) {
+  if (!status_words || timeout_us < 1 || timeout_us > 2000000u || !aligned16(status_words)) return MLA_ERR_INVALID_ARG;
+  if (launch_debug_wait_timeout(1000ull * timeout_us, status_words, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  uint32_t words[2] = {0, 0};
+  if (cudaMemcpy(words, status_words, sizeof words, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  return (words[0] & kErrTimeout) && (words[1] & kErrTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
+}
+
 mla_status_t mla_workspace_status(const void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!workspace || workspace_bytes < sizeof(WsHeader)) return MLA_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;

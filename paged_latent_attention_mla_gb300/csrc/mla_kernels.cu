@@ -110,6 +110,40 @@ cudaError_t launch_reduce(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ debug wait timeout
+// One 2-CTA cluster: tensor memory allocated, then a bounded wait on an mbarrier that
+// nothing arrives at.  The wait gives up after timeout_ns, the CTAs meet, free the tensor
+// memory and report the timeout bit in their status words.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64, 1) debug_wait_timeout_kernel(uint64_t timeout_ns,
+                                                                                           uint32_t* status_words) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc<2>(smem_addr(&tmem_slot), 32);
+    tmem_relinquish<2>();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  uint32_t err = 0;
+  if (tid == 0 && !mbar_wait_bounded(smem_addr(&bar), 0, timeout_ns)) err = kErrTimeout;
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<2>(tmem_slot, 32);
+  if (tid == 0) status_words[cluster_ctarank()] = err;
+}
+
+cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, uint32_t* status_words, cudaStream_t stream) {
+  debug_wait_timeout_kernel<<<2, 64, 0, stream>>>(timeout_ns, status_words);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ debug mask
 __global__ void debug_mask_kernel(const int32_t* seq_lens, int Sq, int causal, int window_left, int max_k,
                                   uint32_t* bits) {

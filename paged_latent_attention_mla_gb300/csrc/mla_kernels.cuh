@@ -7,6 +7,7 @@
 
 namespace mla {
 
+cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, uint32_t* status_words, cudaStream_t stream);
 cudaError_t launch_debug_mask(const int32_t* seq_lens, int B, int Sq, int causal, int window_left, int max_k,
                               uint32_t* bits, cudaStream_t stream);
 cudaError_t launch_debug_gather(const KvMaps& maps, bool e4m3, const int32_t* page_table, const int32_t* seq_lens,

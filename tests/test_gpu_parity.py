@@ -161,3 +161,36 @@ def test_bad_page_id_is_flagged_not_faulted():
     dec(d["q_latent"], d["q_rope"], d["ckv"], d["kpe"], d["page_table"], d["seq_lens"], d["scale"])
     torch.cuda.synchronize()
     assert dec.status() == n.MLA_OK
+
+
+# Larger shapes on sampled rows: a row split over every cluster, the largest query block,
+# many short rows per cluster, e4m3 under a sliding window.
+SAMPLED = {
+    "one_long_request": (dict(H=128, Sq=1, seq_lens=[131072]), 24),
+    "sq64_causal": (dict(H=16, Sq=64, causal=True, seq_lens=[3000, 64, 700]), 40),
+    "many_short_rows": (dict(H=128, Sq=1, seq_lens=[1 + (37 * i) % 300 for i in range(2048)]), 40),
+    "e4m3_window_sq3": (dict(H=128, Sq=3, causal=True, window_left=1000, dtype="e4m3",
+                             seq_lens=[9000, 2, 1500, 40000]), 40),
+}
+
+
+@pytest.mark.parametrize("name", list(SAMPLED))
+def test_larger_shapes_sampled_rows(name):
+    kw, nrows = SAMPLED[name]
+    prob = wl.make_problem("uniform", seed=4321, **kw)
+    O, L = run_gpu(prob)
+    check(prob, O, L, rows=wl.sample_rows(prob, nrows))
+    assert np.isfinite(O).all()
+
+
+def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
+    """A device wait on a barrier nothing arrives at gives up after its limit, the kernel
+    unwinds (peer meeting, tensor memory freed) and reports MLA_ERR_TIMEOUT; the next
+    decode in the same context is still correct."""
+    words = torch.zeros(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(n.MlaError) as e:
+        n.mla_debug_wait_timeout(20000, words)  # 20 ms
+    assert e.value.status == n.MLA_ERR_TIMEOUT
+    prob = wl.make_problem("tiny")
+    O, L = run_gpu(prob)
+    check(prob, O, L)
