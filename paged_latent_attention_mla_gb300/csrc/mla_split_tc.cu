@@ -11,9 +11,9 @@
 //   warps 4-7  correction: rescale O when the row max moves, final epilogue
 //   warp 8     MMA issue (leader CTA, one thread) and TMEM allocation
 //   warp 9     TMA loads of Q (once per piece of work)
-//   warp 10    TMA loads of K blocks and V pages into one ring of 16 KB slots,
-//              in exactly the order the MMAs consume them, page ids read a tile ahead
-//   warp 11    idle
+//   warps 10-11 TMA loads of K blocks and V pages into one ring of 16 KB slots,
+//              in exactly the order the MMAs consume them (even fills by warp 10,
+//              odd fills by warp 11), page ids read a tile ahead
 // P.V takes P as an A operand in tensor memory, where lane half h of a CTA reads
 // its rows from its own lanes: S leaves keys [0, 128) of a row in the lower half
 // and keys [128, 256) in the upper half, so each softmax thread writes its own
@@ -63,7 +63,8 @@ struct Cfg {
   // slot each: this CTA's 128 keys x 128 B) and its V pages (this CTA's columns of 64
   // keys: two slots in bf16, one per output chunk; one slot in e4m3).
   static constexpr int kSlot = 16384;
-  static constexpr int kNS = E4M3 ? 10 : 8;
+  static constexpr int kNS = E4M3 ? 10 : 8;  // even: each loader warp owns every other slot
+  static_assert(kNS % 2 == 0, "the two loader warps own alternate slots");
   static constexpr int kVItems = E4M3 ? 1 : 2;    // ring slots per V page
   static constexpr int kPvSteps = E4M3 ? 2 : 4;  // MMAs per page and output chunk (32 or 16 keys each)
   static constexpr uint32_t kIdescQK = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 0);
@@ -83,10 +84,10 @@ struct Misc {
   // tile ahead of the correction and of the P.V, never two
   uint64_t pv_ready[2];   // leader: one arrival per CTA, P written and O corrected for the next P.V
   uint64_t pv_local[2];   // this CTA's 4 softmax + 4 correction warps, forwarded to the leader's pv_ready
-  uint64_t tail_ready;    // leader: the peer zeroed the tail of a request's last page
+  uint64_t tail_ready;    // leader: the peer zeroed the tail of a request's last page (one arrival a slot)
   uint64_t o_done[2];     // P.V of a tile complete
   uint64_t cor_ready[2];  // softmax -> correction: the tile's rescale factor is posted
-  uint64_t tail_bar, xchg_bar;
+  uint64_t tail_bar[2], xchg_bar;  // tail_bar: one per loader warp
   float xchg[2][128];             // per-tile row-max exchange between the two halves of a row
   float xsum[128];                // final row-sum exchange
   float corr[2][128];             // per-tile rescale factor, softmax -> correction
@@ -120,6 +121,9 @@ __device__ __forceinline__ bool kwait(Misc& M, uint32_t bar, uint32_t parity) {
     }
   }
 }
+
+// the same wait out of line, for call sites whose fast path is inlined
+__device__ __noinline__ bool kwait_slow(Misc& M, uint32_t bar, uint32_t parity) { return kwait(M, bar, parity); }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
@@ -200,8 +204,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&M.o_done[i]), 1);
       mbar_init(smem_addr(&M.cor_ready[i]), 4);
     }
-    mbar_init(smem_addr(&M.tail_ready), 1);
-    mbar_init(smem_addr(&M.tail_bar), 1);
+    mbar_init(smem_addr(&M.tail_ready), C::kVItems);
+    mbar_init(smem_addr(&M.tail_bar[0]), 1);
+    mbar_init(smem_addr(&M.tail_bar[1]), 1);
     mbar_init(smem_addr(&M.xchg_bar), 4);
     fence_mbar_init();
   }
@@ -481,15 +486,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue (leader CTA)
     if (rank == 0 && lane == 0) {
-      int j = 0, pvc = 0, fill = 0, tcount = 0;
+      int j = 0, pvc = 0, tcount = 0;
+      int rslot = 0;        // next ring slot in consumption order
+      uint32_t rphase = 0;  // and the parity of its fill
       int npages = 0, tail_rows = 0;  // of the current piece's request
       bool ok = true;
-      // next ring slot in consumption order: wait until both CTAs' data landed
+      // next ring slot: wait until both CTAs' copies landed (one CTA-scope test in the
+      // common case, the bounded wait otherwise)
       auto take = [&](uint32_t& addr, int& slot) -> bool {
-        slot = fill % C::kNS;
-        if (!kwait(M, smem_addr(&M.full[slot]), (fill / C::kNS) & 1)) return false;
+        slot = rslot;
+        const uint32_t bar = smem_addr(&M.full[rslot]);
+        if (!mbar_try_wait_cta(bar, rphase) && !kwait_slow(M, bar, rphase)) return false;
         addr = sRing + slot * C::kSlot;
-        ++fill;
+        if (++rslot == C::kNS) {
+          rslot = 0;
+          rphase ^= 1u;
+        }
         return true;
       };
       auto qk = [&](int jt) -> bool {
@@ -498,25 +510,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // MMAs in issue order: no separate wait
         const int st = jt & 1;
         const uint32_t d = tmem + st * 128;
-#pragma unroll 1
+        // the descriptors of step t are the block's plus 32 bytes per step
+#pragma unroll E4M3 ? 5 : 1
         for (int kb = 0; kb < C::kNKb; ++kb) {
           uint32_t ka;
           int slot;
           if (!take(ka, slot)) return false;
           tc_fence_after();
-          const bool rope = kb == C::kNLat;
-          const int steps = rope ? C::kRopeSteps : 4;
           const uint32_t qa = sQ + kb * 8192;
-          for (int t = 0; t < steps; ++t) {
-            uint64_t ad, bd;
-            if (E4M3 && rope) {
-              ad = smem_desc_sw64(qa + 32 * t, 512);
-              bd = smem_desc_sw64(ka + 32 * t, 512);
-            } else {
-              ad = smem_desc_sw128(qa + 32 * t, 16, 1024);
-              bd = smem_desc_sw128(ka + 32 * t, 16, 1024);
-            }
-            mma_ss<2, KIND>(d, ad, bd, C::kIdescQK, (kb | t) != 0 ? 1u : 0u);
+          if (E4M3 && kb == C::kNLat) {
+            const uint64_t ad = smem_desc_sw64(qa, 512), bd = smem_desc_sw64(ka, 512);
+#pragma unroll
+            for (int t = 0; t < C::kRopeSteps; ++t) mma_ss<2, KIND>(d, ad + 2 * t, bd + 2 * t, C::kIdescQK, 1u);
+          } else {
+            const uint64_t ad = smem_desc_sw128(qa, 16, 1024), bd = smem_desc_sw128(ka, 16, 1024);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              mma_ss<2, KIND>(d, ad + 2 * t, bd + 2 * t, C::kIdescQK, (kb | t) != 0 ? 1u : 0u);
           }
           mma_commit_pair(smem_addr(&M.empty[slot]), 0x3);
         }
@@ -532,6 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // bf16: slot c holds the columns of output chunk c; e4m3: one slot holds both
           uint32_t va[2];
           int slot[2];
+#pragma unroll
           for (int it = 0; it < C::kVItems; ++it)
             if (!take(va[it], slot[it])) return false;
           if (4 * tile + vp == npages - 1 && tail_rows != 0) {
@@ -540,16 +551,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++tcount;
           }
           tc_fence_after();
+          // output chunk c's V columns: e4m3 at 8 KB into the page's slot, bf16 in slot c;
+          // step t moves 16 (bf16) or 32 (e4m3) keys of 128 B down
+          const uint64_t vd0 = smem_desc_sw128(va[0], 8192, 1024);
+          const uint64_t vd1 = E4M3 ? vd0 + (8192 >> 4) : smem_desc_sw128(va[1], 8192, 1024);
+#pragma unroll
           for (int t = 0; t < C::kPvSteps; ++t) {
             const uint32_t acc = (first && vp == 0 && t == 0) ? 0u : 1u;
             // keys [64 vp + (32 or 16) t, ...) of P: 8 columns of stage pst per step
             const uint32_t a_tm = tmem + pst * 128 + (C::kPCols / 4) * vp + 8 * t;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const uint32_t vb = E4M3 ? va[0] + c * 8192 + t * 4096 : va[c] + t * 2048;
-              mma_ts<2, KIND>(tmem + 256 + 128 * c, a_tm, smem_desc_sw128(vb, 8192, 1024), C::kIdescPV, acc);
-            }
+            const uint64_t dt = static_cast<uint64_t>(t) * ((E4M3 ? 4096 : 2048) >> 4);
+            mma_ts<2, KIND>(tmem + 256, a_tm, vd0 + dt, C::kIdescPV, acc);
+            mma_ts<2, KIND>(tmem + 384, a_tm, vd1 + dt, C::kIdescPV, acc);
           }
+#pragma unroll
           for (int it = 0; it < C::kVItems; ++it) mma_commit_pair(smem_addr(&M.empty[slot[it]]), 0x3);
         }
         mma_commit_pair(smem_addr(&M.o_done[pst]), 0x3);
@@ -588,18 +603,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tma_load_3d_pair(sQ + C::kNLat * 8192, &maps.q_rope, 0, 64 * rank, row, bar);
       }
     }
-  } else if (warp == 10) {
+  } else if (warp >= 10) {
     // ------------------------------------------------------------ K blocks and V pages, one ring
     // Consumption order of each piece: K(t0), then K(t), V(t - 1) for the following tiles,
     // then V(last); a K block is this CTA's two pages x 128 B of columns, a V page this CTA's
-    // output columns of one page.
+    // output columns of one page.  Two warps issue the copies: warp 10 the even fills, warp
+    // 11 the odd ones.  The slot count is even, so a slot always has the same owner, and an
+    // owner only ever waits for the release of its own previous fill of the slot.
+    const int own = warp - 10;
     int fill = 0;
     uint32_t tph = 0;
     bool ok = true;
-    // wait for the next free slot (lane-uniform)
-    auto acquire = [&](int& slot) -> bool {
+    // the next fill in consumption order: this warp's (wait until its slot is free) or the
+    // other warp's (skip); lane-uniform
+    auto acquire = [&](int& slot, bool& mine) -> bool {
       slot = fill % C::kNS;
-      if (fill >= C::kNS && !kwait(M, smem_addr(&M.empty[slot]), ((fill / C::kNS) - 1) & 1)) return false;
+      mine = (fill & 1) == own;
+      if (mine && fill >= C::kNS && !kwait(M, smem_addr(&M.empty[slot]), ((fill / C::kNS) - 1) & 1)) return false;
       ++fill;
       return true;
     };
@@ -620,8 +640,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       auto load_k = [&](int tile, const int (&pg)[4]) -> bool {
         for (int kb = 0; kb < C::kNKb; ++kb) {
           int slot;
-          if (!acquire(slot)) return false;
-          if (lane == 0) {
+          bool mine;
+          if (!acquire(slot, mine)) return false;
+          if (mine && lane == 0) {
             const bool rope = kb == C::kNLat;
             const uint32_t bar = lead(M.full[slot]);
             const uint32_t dst = sRing + slot * C::kSlot;
@@ -640,15 +661,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       auto load_v = [&](int tile, const int (&pg)[4]) -> bool {
         for (int vp = 0; vp < 4; ++vp) {
           int slot[2];
-          for (int it = 0; it < C::kVItems; ++it)
-            if (!acquire(slot[it])) return false;
-          const bool tail = 4 * tile + vp == npages - 1 && tail_rows != 0;
+          bool mine[2];
+          int nmine = 0;
+          for (int it = 0; it < C::kVItems; ++it) {
+            if (!acquire(slot[it], mine[it])) return false;
+            nmine += mine[it] ? 1 : 0;
+          }
+          const bool tail = 4 * tile + vp == npages - 1 && tail_rows != 0 && nmine != 0;
           // this CTA's 128-byte column blocks of V: bf16 blocks {0,1,4,5} or {2,3,6,7}
           // (two per slot, one slot per output chunk), e4m3 blocks {rank, 2 + rank}
           if (lane == 0) {
-            const uint32_t tbar = smem_addr(&M.tail_bar);
-            if (tail) mbar_arrive_expect_tx(tbar, C::kVItems * C::kSlot);
+            const uint32_t tbar = smem_addr(&M.tail_bar[own]);
+            if (tail) mbar_arrive_expect_tx(tbar, nmine * C::kSlot);
             for (int it = 0; it < C::kVItems; ++it) {
+              if (!mine[it]) continue;
               const uint32_t dst = sRing + slot[it] * C::kSlot;
               const uint32_t bar = lead(M.full[slot[it]]);
               if (!tail && rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot[it]]), 2 * C::kSlot);
@@ -664,18 +690,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // last page of the request: each CTA lands it locally and zeroes the slots past
             // its length; the leader then completes its slots' phases, the peer reports on
             // tail_ready (the MMA waits for both on this page)
-            if (!kwait(M, smem_addr(&M.tail_bar), tph & 1)) return false;
+            if (!kwait(M, smem_addr(&M.tail_bar[own]), tph & 1)) return false;
             ++tph;
             for (int it = 0; it < C::kVItems; ++it)
-              for (int u = 0; u < 2; ++u)
-                zero_block_rows(smem + C::kOffRing + slot[it] * C::kSlot + u * 8192, tail_rows, lane, 32);
+              if (mine[it])
+                for (int u = 0; u < 2; ++u)
+                  zero_block_rows(smem + C::kOffRing + slot[it] * C::kSlot + u * 8192, tail_rows, lane, 32);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (rank == 0)
-                for (int it = 0; it < C::kVItems; ++it) mbar_arrive(smem_addr(&M.full[slot[it]]));
-              else
-                mbar_arrive_cluster(lead(M.tail_ready));
+              for (int it = 0; it < C::kVItems; ++it) {
+                if (!mine[it]) continue;
+                if (rank == 0)
+                  mbar_arrive(smem_addr(&M.full[slot[it]]));
+                else
+                  mbar_arrive_cluster(lead(M.tail_ready));
+              }
             }
             __syncwarp();
           }
