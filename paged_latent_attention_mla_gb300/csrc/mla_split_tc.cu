@@ -511,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int st = jt & 1;
         const uint32_t d = tmem + st * 128;
         // the descriptors of step t are the block's plus 32 bytes per step
-#pragma unroll E4M3 ? 5 : 1
+#pragma unroll
         for (int kb = 0; kb < C::kNKb; ++kb) {
           uint32_t ka;
           int slot;
