@@ -37,6 +37,20 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
     const float4* po = reinterpret_cast<const float4*>(p.ws + L.partial_o) +
                        ((size_t)ri.first_slot * (kDLatent / 4) + (d0 + 32 * dg) / 4) * kHeadsPad + h;
     const int np = ri.n_parts;
+    // two pieces per round; each round's partial loads are issued before its weights are
+    // known (the first round's before the LSE arithmetic).  An empty piece (LSE -inf, slot
+    // never written) gets weight 0 and is selected away.
+    float4 x[2][8];
+    auto load_round = [&](int i0) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + u < np ? i0 + u : i0;
+        const float4* src = po + (size_t)i * (kDLatent / 4) * kHeadsPad;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[u][q] = __ldcs(src + (size_t)q * kHeadsPad);
+      }
+    };
+    load_round(0);
     // the pieces' LSEs: loads issued together, then max and sum
     float mx = -INFINITY;
 #pragma unroll 4
@@ -46,31 +60,23 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
 #pragma unroll 4
     for (int i = 0; i < np; ++i) sum += exp2f(plse[(size_t)i * kHeadsPad] - m0);
     lse2 = sum > 0.f ? m0 + log2f(sum) : -INFINITY;
-    if (sum > 0.f) {
-      // two pieces per round, their loads issued before any use; an empty piece (LSE -inf,
-      // slot never written) gets weight 0 and is selected away
-      for (int i0 = 0; i0 < np; i0 += 2) {
-        float4 x[2][8];
-        float w[2];
+    for (int i0 = 0; i0 < np; i0 += 2) {
+      if (i0 > 0) load_round(i0);
+      float w[2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int i = i0 + u < np ? i0 + u : i0;
-          const float li = plse[(size_t)i * kHeadsPad];
-          w[u] = (i0 + u < np && li != -INFINITY) ? exp2f(li - lse2) : 0.f;
-          const float4* src = po + (size_t)i * (kDLatent / 4) * kHeadsPad;
+      for (int u = 0; u < 2; ++u) {
+        const float li = plse[(size_t)(i0 + u < np ? i0 + u : i0) * kHeadsPad];
+        w[u] = (sum > 0.f && i0 + u < np && li != -INFINITY) ? exp2f(li - lse2) : 0.f;
+      }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) x[u][q] = __ldcs(src + (size_t)q * kHeadsPad);
-        }
+      for (int u = 0; u < 2; ++u) {
+        if (w[u] == 0.f) continue;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (w[u] == 0.f) continue;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            acc[4 * q] += w[u] * x[u][q].x;
-            acc[4 * q + 1] += w[u] * x[u][q].y;
-            acc[4 * q + 2] += w[u] * x[u][q].z;
-            acc[4 * q + 3] += w[u] * x[u][q].w;
-          }
+        for (int q = 0; q < 8; ++q) {
+          acc[4 * q] += w[u] * x[u][q].x;
+          acc[4 * q + 1] += w[u] * x[u][q].y;
+          acc[4 * q + 2] += w[u] * x[u][q].z;
+          acc[4 * q + 3] += w[u] * x[u][q].w;
         }
       }
     }
