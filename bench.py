@@ -40,11 +40,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FLOP_PER_KEY_HEAD = 2 * (576 + 512)  # QK^T over 576 dims + P.V over 512 dims
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one split-KV kernel launch,
-# from an ncu capture of the same command (profiles/split_kv_tc_uniform.md), valid only for
+# from an ncu capture of the same command (profiles/split_kv_tc_uniform.md, split_kv_tc_fp8spec.md), valid only for
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "c869aa2c0576f43eac1da8f6d61cb62ad586e332c9fe940b13b8cdfeb591abb0", "bytes": 322029056 + 14751488},
+    "uniform": {"sources_sha256": "0b5d8856969374668e610c7e1d122c3f7c9cdf88e88df37da6b4e31c950a26fe", "bytes": 321433344 + 14914304},
+    "fp8spec": {"sources_sha256": "0b5d8856969374668e610c7e1d122c3f7c9cdf88e88df37da6b4e31c950a26fe", "bytes": 569635072 + 17697024},
 }
 
 
