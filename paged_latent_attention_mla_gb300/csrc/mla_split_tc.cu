@@ -581,10 +581,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int i = 0; i < n && ok; ++i) {
           ok = qk(j + i);
+          // Q is free once the piece's last QK^T completes: the next piece's Q load need
+          // not wait for the P.V issued after it
+          if (ok && i == n - 1) mma_commit_pair(smem_addr(&M.q_empty), 0x3);
           if (ok && i >= 1) ok = pv(i == 1, sg.tile_begin + i - 1);
         }
         if (!ok) break;
-        mma_commit_pair(smem_addr(&M.q_empty), 0x3);
         ok = pv(n == 1, sg.tile_end - 1);
         j += n;
       }
