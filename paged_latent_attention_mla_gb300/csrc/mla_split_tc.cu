@@ -227,7 +227,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = M.tmem_base;
   const int nseg = M.nseg;
   auto lead = [&](uint64_t& bar) { return map_to_rank(smem_addr(&bar), 0); };
-  const float ln2 = 0.69314718055994530942f;
 
   if (warp < 4) {
     // ------------------------------------------------------------ softmax
