@@ -44,8 +44,8 @@ FLOP_PER_KEY_HEAD = 2 * (576 + 512)  # QK^T over 576 dims + P.V over 512 dims
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "0b5d8856969374668e610c7e1d122c3f7c9cdf88e88df37da6b4e31c950a26fe", "bytes": 321433344 + 14914304},
-    "fp8spec": {"sources_sha256": "0b5d8856969374668e610c7e1d122c3f7c9cdf88e88df37da6b4e31c950a26fe", "bytes": 569635072 + 17697024},
+    "uniform": {"sources_sha256": "96ece8eb2eb630649a03b07bb010fd64c0cf0457aa1d9bd6da07b9512113d238", "bytes": 321266688 + 14566400},
+    "fp8spec": {"sources_sha256": "96ece8eb2eb630649a03b07bb010fd64c0cf0457aa1d9bd6da07b9512113d238", "bytes": 568142592 + 17271808},
 }
 
 
