@@ -308,6 +308,17 @@ def run_ours(args, world, rank, local_rank):
         e_ms.append(a.elapsed_time(b))
     e2e_ms = max_over_ranks(statistics.mean(e_ms))
 
+    # the same device-resident call back to back with no L2 flush between calls (part of
+    # the KV can then still be in L2 from the previous call): reported beside the number
+    nf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in nf:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    nf_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in nf))
+
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
@@ -355,6 +366,7 @@ def run_ours(args, world, rank, local_rank):
         "clocks": clk.summary(),
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "no_flush": {"us_per_call": nf_ms * 1e3, "l2": "not flushed between calls"},
         "gpu_launches": launches,
         "cpu_baseline": ({k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")} if cb else None),
     }
