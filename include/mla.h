@@ -53,7 +53,7 @@ extern "C" {
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,         /* a NULL / misaligned pointer, a bad size or shape */
-  MLA_ERR_UNSUPPORTED = 2,         /* valid, but outside what this build implements */
+  MLA_ERR_UNSUPPORTED = 2,         /* valid, but outside what the library implements */
   MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < what mla_plan reported */
   MLA_ERR_CUDA = 4,                /* a CUDA runtime call failed (launch or an earlier fault) */
   MLA_ERR_TIMEOUT = 5              /* a bounded device wait gave up (read by mla_workspace_status) */
@@ -106,7 +106,7 @@ typedef struct {
  *
  *  seq_lens        host [B] int32, 0 <= seq_lens[b] <= page_table_stride * page_size
  *  B, H            requests and heads, 1 <= H <= 128
- *  page_size       keys per page: 64 (the only size this build supports)
+ *  page_size       keys per page: 64 (the only size the library supports)
  *  window_left     -1 for full history, else >= 0
  *  cfg             tensor metadata as above
  *  split_kv        out: the most pieces any row is split into (1 = no reduction needed)
