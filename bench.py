@@ -1,9 +1,11 @@
 """Benchmark: paged MLA decode on GB300, one JSON line on rank 0.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload uniform] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all] [--impl ours|reference]
 
 A step is one mla_decode call (split-KV kernel + reduction) over one synthetic
-decode batch resident in HBM.  L2 is flushed (a 256 MB device write, outside
+decode batch resident in HBM.  The headline value is the uniform batch; the
+default run also measures the varlen, fp8spec and window batches and reports
+each under "workloads" with its own roofline record.  L2 is flushed (a 256 MB device write, outside
 the timed events) before every timed step.  Under torchrun every rank decodes
 its own batch of the same shape (requests are independent: weak scaling, no
 collective on the data path); the step time is the maximum over ranks.
@@ -38,6 +40,8 @@ from paged_latent_attention_mla_gb300.sharding import max_over_ranks, rank_seed 
 METRIC = "MLA decode µs/call, TFLOP/s and KV HBM GB/s vs GB300 roofline fraction"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLOP_PER_KEY_HEAD = 2 * (576 + 512)  # QK^T over 576 dims + P.V over 512 dims
+HEADLINE = "uniform"  # the headline value; the other 128-head workloads get records beside it
+ALL = ["uniform", "varlen", "fp8spec", "window"]
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one split-KV kernel launch,
 # from an ncu capture of the same command (profiles/split_kv_tc_uniform.md, split_kv_tc_fp8spec.md), valid only for
@@ -162,26 +166,27 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(prob, budget_s: float = 12.0):
+def cpu_baseline(prob, budget_s: float = 12.0, threads: int = 0):
     """The oracle as it stands, on this host's cores, over a bounded sample of rows."""
     import oracle
 
     p = prob.host_inputs()
     total = prob.B * prob.Sq * prob.H
-    cores = oracle.max_threads()
+    cores = threads if threads > 0 else len(os.sched_getaffinity(0))
     rows = wl.sample_rows(prob, min(total, 4 * cores))
     t0 = time.perf_counter()
-    oracle.decode(p, rows=rows)
+    oracle.decode(p, rows=rows, threads=cores)
     dt = time.perf_counter() - t0
     n = min(total, max(len(rows), int(len(rows) * budget_s / max(dt, 1e-3))))
     if n > len(rows):
         rows = wl.sample_rows(prob, n, seed=11)
         t0 = time.perf_counter()
-        oracle.decode(p, rows=rows)
+        oracle.decode(p, rows=rows, threads=cores)
         dt = time.perf_counter() - t0
     flops = row_flops(prob, rows)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} of {total} (request, token, head) rows, every visible key, fp64 oracle, {dt:.2f} s",
+            "sample": f"{len(rows)} of {total} (request, token, head) rows, every visible key, fp64 oracle, "
+                      f"{cores} thread(s), {dt:.2f} s",
             "seconds": dt}
 
 
@@ -203,8 +208,7 @@ def row_flops(prob, rows):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    prob = wl.make_problem(args.workload)
-    flops, kv = algorithmic_counts(prob)
+    prob = wl.make_problem(HEADLINE if args.workload == "all" else args.workload)
     times = []
     cb = None
     per_step = min(args.ref_budget, 150.0 / max(1, args.warmup + args.steps))  # whole run within a few minutes
@@ -222,11 +226,14 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local_rank):
-    torch.cuda.set_device(local_rank)
-    nbuild.build()
-    _native.load()
-    prob = wl.make_problem(args.workload, seed=rank_seed(wl.WORKLOADS[args.workload].seed, rank))
+def ev_pair():
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def measure(name, args, world, rank, local_rank, peaks, peak_src):
+    """One workload: the device-resident call (L2 flushed before each), the split-KV kernel
+    alone, the call through host buffers, and the call without the flush."""
+    prob = wl.make_problem(name, seed=rank_seed(wl.WORKLOADS[name].seed, rank))
     d = prob.device_inputs("cuda")
     dec = decoder_for(prob)
     flops, kv = algorithmic_counts(prob)
@@ -243,11 +250,11 @@ def run_ours(args, world, rank, local_rank):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
-    assert dec.status() == _native.MLA_OK, "decode reported an error during warm-up"
+    assert dec.status() == _native.MLA_OK, f"{name}: decode reported an error during warm-up"
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [ev_pair() for _ in range(args.steps)]
     # the split-KV kernel alone: mla_decode records these around its launch (split_timing)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [ev_pair() for _ in range(args.steps)]
     for a, b in kev:  # create the handles
         a.record(stream)
         b.record(stream)
@@ -273,15 +280,15 @@ def run_ours(args, world, rank, local_rank):
         torch.cuda.synchronize()
     dec.cfg.split_timing[0] = None
     dec.cfg.split_timing[1] = None
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    ms_max = max_over_ranks(ms)
+    assert dec.status() == _native.MLA_OK, f"{name}: decode reported an error"
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev))
     kernel_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in kev))
-    launches = 2 * args.steps  # split-KV kernel + reduction per decode call
 
     # end to end through the public API with host buffers: H2D of the step's queries,
     # page table and lengths from pinned memory, decode, D2H of out and lse
-    hq = [d[k].cpu().pin_memory() for k in ("q_latent", "q_rope", "page_table", "seq_lens")]
-    dq = [torch.empty_like(d[k]) for k in ("q_latent", "q_rope", "page_table", "seq_lens")]
+    keys = ("q_latent", "q_rope", "page_table", "seq_lens")
+    hq = [d[k].cpu().pin_memory() for k in keys]
+    dq = [torch.empty_like(d[k]) for k in keys]
     h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in hq)
@@ -300,7 +307,7 @@ def run_ours(args, world, rank, local_rank):
     e_ms = []
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = ev_pair()
         a.record(stream)
         e2e_step()
         b.record(stream)
@@ -310,7 +317,7 @@ def run_ours(args, world, rank, local_rank):
 
     # the same device-resident call back to back with no L2 flush between calls (part of
     # the KV can then still be in L2 from the previous call): reported beside the number
-    nf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    nf = [ev_pair() for _ in range(args.steps)]
     torch.cuda.synchronize()
     for a, b in nf:
         a.record(stream)
@@ -318,57 +325,87 @@ def run_ours(args, world, rank, local_rank):
         b.record(stream)
     torch.cuda.synchronize()
     nf_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in nf))
+    launches_per_call = dec.launches_per_call()
 
-    if rank != 0:
-        return
-    peaks, peak_src = load_peaks()
-    tflops_rank = flops / (ms_max * 1e-3) / 1e12
-    kv_gbs = kv / (ms_max * 1e-3) / 1e9
     t_hbm = kv / (peaks["hbm_gbs"] * 1e9)
-    # e4m3 contractions run at twice the bf16 tensor rate (nominal ratio 4.5 / 2.25 PFLOP/s)
-    tc_peak = peaks["bf16_tflops"] * (2.0 if prob.w.dtype == "e4m3" else 1.0)
+    e4m3 = prob.w.dtype == "e4m3"
+    tc_peak = peaks["bf16_tflops"] * (2.0 if e4m3 else 1.0)
     t_tc = flops / (tc_peak * 1e12)
+    t_roof = max(t_hbm, t_tc)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    # the dominant kernel (split-KV) timed alone by its own events
     k_gbs = kv / (kernel_ms * 1e-3) / 1e9
     k_tflops = flops / (kernel_ms * 1e-3) / 1e12
+    src = "MEASURED_PEAKS.json" if peak_src == "measured" else "the profiling recipe's fallback"
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": k_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": k_gbs / peaks["hbm_gbs"]}
+                "frac": k_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src}: hbm_gbs of {src}"}
     else:
         roof = {"bound": "tensor", "achieved": k_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": k_tflops / tc_peak}
-    roof.update({"traffic": measured_traffic(args.workload), "kernel": "split_kv_tc (the split-KV kernel of mla_decode)",
-                 "kernel_us": kernel_ms * 1e3,
-                 "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
-                 "t_roofline_us": 1e6 * max(t_hbm, t_tc)})
-    cb = cpu_baseline(prob, budget_s=args.cpu_budget) if args.cpu_budget > 0 else None
+                "frac": k_tflops / tc_peak,
+                "peak_source": (f"{peak_src}: 2 x bf16_tflops of {src} (burst); e4m3 is not measured on its own, "
+                                "2x is the nominal e4m3/bf16 dense ratio (4.5 / 2.25 PFLOP/s)") if e4m3 else
+                               f"{peak_src}: bf16_tflops of {src} (burst)"}
+    roof.update({"traffic": measured_traffic(name), "kernel": "split_kv_tc (the split-KV kernel of mla_decode)",
+                 "kernel_us": kernel_ms * 1e3, "t_roofline_us": 1e6 * t_roof,
+                 # the whole call (split-KV kernel and reduction) against the same roofline
+                 "frac_call": (1e6 * t_roof) / (ms * 1e3)})
+    rec = {"workload": describe(prob), "us_per_call": ms * 1e3, "kernel_us": kernel_ms * 1e3,
+           "tflops": world * flops / (ms * 1e-3) / 1e12, "kv_gbs": world * kv / (ms * 1e-3) / 1e9,
+           "flops_per_step": flops, "kv_bytes_per_step": kv, "dtype": prob.w.dtype, "roofline": roof,
+           "clocks": clk.summary(),
+           "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+           "no_flush": {"us_per_call": nf_ms * 1e3, "l2": "not flushed between calls"},
+           "gpu_launches": launches_per_call * args.steps, "ms": ms}
+    del d, dec, flush, out, lse, hq, dq
+    torch.cuda.empty_cache()
+    return prob, rec
+
+
+def run_ours(args, world, rank, local_rank):
+    torch.cuda.set_device(local_rank)
+    nbuild.build()
+    _native.load()
+    peaks, peak_src = load_peaks()
+    names = ALL if args.workload == "all" else [args.workload]
+    head = HEADLINE if HEADLINE in names else names[0]
+    records, probs = {}, {}
+    for name in names:
+        probs[name], records[name] = measure(name, args, world, rank, local_rank, peaks, peak_src)
+    if rank != 0:
+        return
+    h = records[head]
+    cb = cb1 = None
+    if args.cpu_budget > 0:
+        cb = cpu_baseline(probs[head], budget_s=args.cpu_budget)
+        cb1 = cpu_baseline(probs[head], budget_s=max(1.0, args.cpu_budget / 3), threads=1)
     line = {
         "metric": METRIC,
-        "value": tflops_rank * world,
+        "value": h["tflops"],
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_max,
-        "us_per_call": ms_max * 1e3,
-        "kv_gbs": kv_gbs * world,
-        "tflops": tflops_rank * world,
+        "ms_per_step": h["ms"],
+        "us_per_call": h["us_per_call"],
+        "kv_gbs": h["kv_gbs"],
+        "tflops": h["tflops"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": prob.w.dtype,
+        "dtype": h["dtype"],
         "data": "synthetic",
-        "config": {"workload": describe(prob), "l2": "flushed before every timed step (256 MB device write)",
-                   "parallelism": f"{world} independent batches (one per GPU)", "flops_per_step": flops,
-                   "kv_bytes_per_step": kv},
-        "roofline": roof,
-        "clocks": clk.summary(),
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "no_flush": {"us_per_call": nf_ms * 1e3, "l2": "not flushed between calls"},
-        "gpu_launches": launches,
+        "config": {"workload": h["workload"], "l2": "flushed before every timed step (256 MB device write)",
+                   "parallelism": f"{world} independent batches (one per GPU)", "flops_per_step": h["flops_per_step"],
+                   "kv_bytes_per_step": h["kv_bytes_per_step"]},
+        "roofline": h["roofline"],
+        "clocks": h["clocks"],
+        "e2e": h["e2e"],
+        "no_flush": h["no_flush"],
+        "gpu_launches": h["gpu_launches"],
         "cpu_baseline": ({k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")} if cb else None),
+        "cpu_baseline_1core": ({k: cb1[k] for k in ("value", "unit", "cores", "kind", "sample")} if cb1 else None),
+        "workloads": {n: {k: v for k, v in r.items() if k != "ms"} for n, r in records.items()},
     }
     print(json.dumps(line), flush=True)
 
@@ -378,7 +415,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="uniform", choices=list(wl.WORKLOADS))
+    ap.add_argument("--workload", default="all", choices=["all"] + list(wl.WORKLOADS),
+                    help="all (default): the uniform headline plus records for varlen, fp8spec and window")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per reference-arm step")

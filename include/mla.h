@@ -155,14 +155,25 @@ MLA_API mla_status_t mla_decode(const void *q_latent, const void *q_rope, const 
  * The array is 64 MiB on every GPU that loads the library, held until the
  * process exits; a batch needing more (see mla_plan's workspace_bytes) returns
  * MLA_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call on a device
- * looks the array's address up, so make it before any stream capture.  All
- * calls share the one array: calls that overlap on the GPU race (serialize them,
- * e.g. on one stream).  Nothing in it needs clearing between calls.
+ * looks the array's address up, so make it before any stream capture; the
+ * address is cached for the life of the device context (after cudaDeviceReset
+ * reload the library).  All calls share the one array: calls that overlap on
+ * the GPU race (serialize them, e.g. on one stream).  Nothing in it needs
+ * clearing between calls.  Device-side errors of a call (see mla_decode) are
+ * read with mla_noalloc_status; the output of a call that reports one is
+ * incomplete.
  */
 MLA_API mla_status_t mla_decode_noalloc(const void *q_latent, const void *q_rope, const void *ckv_cache,
                                         const void *kpe_cache, const int32_t *page_table, const int32_t *seq_lens,
                                         float scale, int window_left, void *out, float *lse, cudaStream_t stream,
                                         int B, int H, int page_size, const mla_config_t *cfg);
+
+/*
+ * Device-side status of the last mla_decode_noalloc on the current device: what
+ * mla_workspace_status reports for a workspace, read from the library's own
+ * array.  Synchronizes the stream.  Not for the decode path.
+ */
+MLA_API mla_status_t mla_noalloc_status(cudaStream_t stream);
 
 /*
  * Debug gather: the decode kernel's page walk and tile load, written back densely.
@@ -195,9 +206,17 @@ MLA_API mla_status_t mla_debug_mask(const int32_t *seq_lens, int B, int window_l
 MLA_API mla_status_t mla_debug_wait_timeout(unsigned timeout_us, uint32_t *status_words, cudaStream_t stream);
 
 /*
- * Debug status: synchronizes the stream and reads the status word that the
- * last mla_decode on this workspace left (MLA_OK, or MLA_ERR_TIMEOUT when a
- * bounded device wait gave up).  Not for the decode path.
+ * Device-side status of the last mla_decode on this workspace: synchronizes the
+ * stream and reads the status words the decode kernel left there.
+ *   MLA_OK               nothing went wrong on the device
+ *   MLA_ERR_TIMEOUT      a bounded device wait gave up (the kernel unwound instead of hanging)
+ *   MLA_ERR_INVALID_ARG  a visible page-table entry outside [0, num_pages) (read as zeros),
+ *                        a device seq_lens value outside [0, page_table_stride * page_size),
+ *                        or a batch that gave one cluster more pieces than it can hold
+ *                        (a batch that mla_plan rejected with MLA_ERR_UNSUPPORTED)
+ * mla_decode cannot see these conditions (it returns once the kernels are
+ * enqueued); the output of a call that reports one is incomplete.  Not for the
+ * decode path.
  */
 MLA_API mla_status_t mla_workspace_status(const void *workspace, size_t workspace_bytes, cudaStream_t stream);
 

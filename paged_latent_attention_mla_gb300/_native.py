@@ -20,7 +20,7 @@ MLA_BF16, MLA_E4M3, MLA_F32 = 0, 1, 2
 
 _DTYPES = {torch.bfloat16: MLA_BF16, torch.float8_e4m3fn: MLA_E4M3, torch.float32: MLA_F32}
 
-EXPORTS = ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_debug_gather", "mla_debug_mask",
+EXPORTS = ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_noalloc_status", "mla_debug_gather", "mla_debug_mask",
            "mla_debug_wait_timeout", "mla_workspace_status", "mla_status_string")
 
 
@@ -72,10 +72,11 @@ def load(path: str | None = None):
             lib.mla_debug_mask.argtypes = [P, I, I, I, cfgp, P, P]
             lib.mla_debug_wait_timeout.argtypes = [ctypes.c_uint, P, P]
             lib.mla_workspace_status.argtypes = [P, S, P]
+            lib.mla_noalloc_status.argtypes = [P]
             lib.mla_status_string.argtypes = [I]
             lib.mla_status_string.restype = ctypes.c_char_p
-            for fn in ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_debug_gather", "mla_debug_mask",
-                       "mla_debug_wait_timeout", "mla_workspace_status"):
+            for fn in ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_noalloc_status", "mla_debug_gather",
+                       "mla_debug_mask", "mla_debug_wait_timeout", "mla_workspace_status"):
                 getattr(lib, fn).restype = I
             _lib = lib
     return _lib
@@ -137,6 +138,11 @@ def mla_decode_noalloc(q_latent, q_rope, ckv_cache, kpe_cache, page_table, seq_l
         _ptr(q_latent), _ptr(q_rope), _ptr(ckv_cache), _ptr(kpe_cache), _ptr(page_table), _ptr(seq_lens),
         float(scale), int(window_left), _ptr(out), _ptr(lse), _stream(stream), int(B), int(H),
         int(ckv_cache.shape[1]), ctypes.byref(cfg)))
+
+
+def mla_noalloc_status(stream=None) -> int:
+    """Device-side status of the last mla_decode_noalloc on the current device (synchronizes)."""
+    return load().mla_noalloc_status(_stream(stream))
 
 
 def mla_debug_gather(ckv_cache, kpe_cache, page_table, seq_lens, max_k: int, dense_out, cfg: MlaConfig, stream=None):

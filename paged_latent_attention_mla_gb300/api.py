@@ -52,6 +52,10 @@ class PagedMlaDecoder:
                            self.workspace, self.cfg, stream)
         return out, lse
 
+    def launches_per_call(self) -> int:
+        """Kernels one decode call launches: the split-KV kernel and the reduction."""
+        return 2
+
     def status(self, stream=None) -> int:
         return _native.mla_workspace_status(self.workspace, stream)
 

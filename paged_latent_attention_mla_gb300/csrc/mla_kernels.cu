@@ -130,8 +130,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64, 1) debug_wait_ti
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc<2>(smem_addr(&tmem_slot), 32);
-    tmem_relinquish<2>();
+    tmem_alloc_pair(smem_addr(&tmem_slot), 32);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   cluster_sync();
@@ -141,7 +141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64, 1) debug_wait_ti
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc<2>(tmem_slot, 32);
+  if (warp == 0) tmem_dealloc_pair(tmem_slot, 32);
   if (tid == 0) status_words[cluster_ctarank()] = err;
 }
 

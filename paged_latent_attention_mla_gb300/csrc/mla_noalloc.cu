@@ -9,9 +9,14 @@
 //
 // The array's address is looked up once per device (cudaGetSymbolAddress, with
 // that device current) on the first call made on it; that first call should come
-// before any stream capture.  Every call shares the array, so calls that overlap
-// on the GPU race; the array keeps the last call's contents, which the decode
-// never reads before writing (nothing needs clearing).
+// before any stream capture.  The cached address belongs to the device context it
+// was looked up in: after cudaDeviceReset (or any teardown of the primary
+// context) the library must be reloaded before these calls are used again.
+// Every call shares the array, so calls that overlap on the GPU race; the array
+// keeps the last call's contents.  A call that completes without a device-side
+// error writes every slot the reduction reads before reading it, so nothing
+// needs clearing; when the kernel reports an error (mla_noalloc_status) the
+// output of that call is incomplete and may mix in an earlier call's partials.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -54,4 +59,12 @@ extern "C" mla_status_t mla_decode_noalloc(const void* q_latent, const void* q_r
   // returns MLA_ERR_WORKSPACE_TOO_SMALL, launching nothing, when it does not fit.
   return mla_decode(q_latent, q_rope, ckv_cache, kpe_cache, page_table, seq_lens, scale, window_left, out, lse, ws,
                     kNoAllocScratchBytes, stream, B, H, page_size, cfg);
+}
+
+// The device-side status of the last mla_decode_noalloc on the current device: the
+// same read mla_workspace_status does, on the library's own array.
+extern "C" mla_status_t mla_noalloc_status(cudaStream_t stream) {
+  void* ws = scratch_address();
+  if (!ws) return MLA_ERR_CUDA;
+  return mla_workspace_status(ws, kNoAllocScratchBytes, stream);
 }

@@ -211,8 +211,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 8) {
-    tmem_alloc<2>(smem_addr(&M.tmem_base), 512);
-    tmem_relinquish<2>();
+    tmem_alloc_pair(smem_addr(&M.tmem_base), 512);
+    tmem_relinquish_pair();
   }
   if (warp == 9 && lane == 0) {
     tma_prefetch_desc(&maps.ckv);
@@ -520,12 +520,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (E4M3 && kb == C::kNLat) {
             const uint64_t ad = smem_desc_sw64(qa, 512), bd = smem_desc_sw64(ka, 512);
 #pragma unroll
-            for (int t = 0; t < C::kRopeSteps; ++t) mma_ss<2, KIND>(d, ad + 2 * t, bd + 2 * t, C::kIdescQK, 1u);
+            for (int t = 0; t < C::kRopeSteps; ++t) mma_ss<KIND>(d, ad + 2 * t, bd + 2 * t, C::kIdescQK, 1u);
           } else {
             const uint64_t ad = smem_desc_sw128(qa, 16, 1024), bd = smem_desc_sw128(ka, 16, 1024);
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              mma_ss<2, KIND>(d, ad + 2 * t, bd + 2 * t, C::kIdescQK, (kb | t) != 0 ? 1u : 0u);
+              mma_ss<KIND>(d, ad + 2 * t, bd + 2 * t, C::kIdescQK, (kb | t) != 0 ? 1u : 0u);
           }
           mma_commit_pair(smem_addr(&M.empty[slot]), 0x3);
         }
@@ -560,8 +560,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // keys [64 vp + (32 or 16) t, ...) of P: 8 columns of stage pst per step
             const uint32_t a_tm = tmem + pst * 128 + (C::kPCols / 4) * vp + 8 * t;
             const uint64_t dt = static_cast<uint64_t>(t) * ((E4M3 ? 4096 : 2048) >> 4);
-            mma_ts<2, KIND>(tmem + 256, a_tm, vd0 + dt, C::kIdescPV, acc);
-            mma_ts<2, KIND>(tmem + 384, a_tm, vd1 + dt, C::kIdescPV, acc);
+            mma_ts<KIND>(tmem + 256, a_tm, vd0 + dt, C::kIdescPV, acc);
+            mma_ts<KIND>(tmem + 384, a_tm, vd1 + dt, C::kIdescPV, acc);
           }
 #pragma unroll
           for (int it = 0; it < C::kVItems; ++it) mma_commit_pair(smem_addr(&M.empty[slot[it]]), 0x3);
@@ -737,7 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc<2>(tmem, 512);
+  if (warp == 8) tmem_dealloc_pair(tmem, 512);
   if (tid == 0) {
     const WsLayout WL = ws_layout(p.B * p.Sq, p.num_clusters);
     reinterpret_cast<uint32_t*>(p.ws + WL.cta_status)[2 * cl + rank] = M.err;

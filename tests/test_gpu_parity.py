@@ -3,9 +3,11 @@
 Tolerances (the decode's stated bar): bf16 inputs, max|O - O*| <= 1e-2 * max|O*|
 and |LSE - LSE*| <= 1e-3; e4m3 inputs, max|O - O*| <= 5e-2 * max|O*| (the LSE is
 checked at 2e-2 there: P is rounded to e4m3 before P.V, the LSE is not, but the
-scores carry e4m3 inputs).  Non-finite values fail.  Small cases are compared
-row by row in full; the five full-size workloads on sampled rows.
+scores carry e4m3 inputs).  Non-finite values fail.  Every case, the full-size
+workloads included, is compared on every (request, token, head) row.
 """
+
+import time
 
 import numpy as np
 import pytest
@@ -105,14 +107,17 @@ def test_repeated_calls_are_deterministic():
     assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
 
 
-@pytest.mark.parametrize("name,nrows", [("uniform", 48), ("varlen", 40), ("fp8spec", 32), ("window", 48)])
-def test_full_size_workloads_sampled_rows(name, nrows):
+@pytest.mark.parametrize("name", ["uniform", "varlen", "fp8spec", "window"])
+def test_full_size_workloads_all_rows(name, record_property):
+    """The benchmarked workloads at full size, in the launch configuration the benchmark
+    times (one persistent wave sized from the device), against the oracle on every row."""
     prob = wl.make_problem(name)
     O, L = run_gpu(prob)
-    rows = wl.sample_rows(prob, nrows)
-    check(prob, O, L, rows=rows)
-    # whole-output sanity at full size: finite everywhere, empty rows exactly zero
-    assert np.isfinite(O).all()
+    t0 = time.perf_counter()
+    err_o, err_l = check(prob, O, L)
+    record_property("oracle_seconds", round(time.perf_counter() - t0, 2))
+    record_property("max_rel_err_o", float(err_o))
+    record_property("max_err_lse", float(err_l))
     del O, L
     torch.cuda.empty_cache()
 
@@ -163,24 +168,22 @@ def test_bad_page_id_is_flagged_not_faulted():
     assert dec.status() == n.MLA_OK
 
 
-# Larger shapes on sampled rows: a row split over every cluster, the largest query block,
+# Larger shapes, every row: a row split over every cluster, the largest query block,
 # many short rows per cluster, e4m3 under a sliding window.
-SAMPLED = {
-    "one_long_request": (dict(H=128, Sq=1, seq_lens=[131072]), 24),
-    "sq64_causal": (dict(H=16, Sq=64, causal=True, seq_lens=[3000, 64, 700]), 40),
-    "many_short_rows": (dict(H=128, Sq=1, seq_lens=[1 + (37 * i) % 300 for i in range(2048)]), 40),
-    "e4m3_window_sq3": (dict(H=128, Sq=3, causal=True, window_left=1000, dtype="e4m3",
-                             seq_lens=[9000, 2, 1500, 40000]), 40),
+LARGER = {
+    "one_long_request": dict(H=128, Sq=1, seq_lens=[131072]),
+    "sq64_causal": dict(H=16, Sq=64, causal=True, seq_lens=[3000, 64, 700]),
+    "many_short_rows": dict(H=128, Sq=1, seq_lens=[1 + (37 * i) % 300 for i in range(2048)]),
+    "e4m3_window_sq3": dict(H=128, Sq=3, causal=True, window_left=1000, dtype="e4m3",
+                            seq_lens=[9000, 2, 1500, 40000]),
 }
 
 
-@pytest.mark.parametrize("name", list(SAMPLED))
-def test_larger_shapes_sampled_rows(name):
-    kw, nrows = SAMPLED[name]
-    prob = wl.make_problem("uniform", seed=4321, **kw)
+@pytest.mark.parametrize("name", list(LARGER))
+def test_larger_shapes_all_rows(name):
+    prob = wl.make_problem("uniform", seed=4321, **LARGER[name])
     O, L = run_gpu(prob)
-    check(prob, O, L, rows=wl.sample_rows(prob, nrows))
-    assert np.isfinite(O).all()
+    check(prob, O, L)
 
 
 def test_bounded_wait_reports_timeout_and_the_context_stays_usable():

@@ -68,7 +68,22 @@ def test_two_calls_in_a_row_match_the_workspace_decode():
         out_ws, lse_ws, cfg = with_workspace(prob, d)
         out_na, lse_na = without_allocation(prob, d, cfg)
         torch.cuda.synchronize()
+        assert n.mla_noalloc_status() == n.MLA_OK
         assert_close(prob, (out_ws, lse_ws), (out_na, lse_na))
+
+
+def test_device_side_errors_are_readable():
+    """A visible page id outside the pool is read as zeros and flagged on the device; the
+    flag is read back from the library's array, and a clean call clears it."""
+    prob = wl.make_problem("uniform", seed=34, H=128, seq_lens=[700, 300])
+    d = prob.device_inputs("cuda")
+    dec = decoder_for(prob)
+    d["page_table"][0, 3] = prob.pool_pages + 11
+    without_allocation(prob, d, dec.cfg)
+    assert n.mla_noalloc_status() == n.MLA_ERR_INVALID_ARG
+    d["page_table"][0, 3] = int(prob.physical_page_table()[0, 3])
+    without_allocation(prob, d, dec.cfg)
+    assert n.mla_noalloc_status() == n.MLA_OK
 
 
 def test_batch_beyond_the_array_is_refused():
