@@ -11,7 +11,10 @@ docs (BlackwellMultiHeadLatentAttentionForwardFP8): ``decode`` is the
 definition (softmax(q.[c;kpe]^T * scale) . c with a natural-log LSE),
 ``decode_split`` the page's split-KV tiling (get_k_tile_count) plus its base-2
 LSE-weighted combine (reduction_kernel), ``gather`` and ``visibility_bits`` the
-page-table walk and the causal / sliding-window visible range.
+page-table walk and the causal / sliding-window visible range.  ``decode_ex``
+adds decode context parallelism (``__init__``'s cp_world, cp_rank and
+cp_interleave_size, ``__call__``'s causal_seqs) and ``__call__``'s
+local_visible_lens; ``merge`` combines the ranks' pieces.
 """
 
 from __future__ import annotations
@@ -53,6 +56,9 @@ def _load():
             P = ctypes.c_void_p
             i, d, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
             lib.oracle_mla_decode.argtypes = [P, P, P, P, i, d, d, d, P, i, P, i, i, i, i, i, d, i, i, P, i64, i, P, P]
+            lib.oracle_mla_decode_ex.argtypes = [P, P, P, P, i, d, d, d, P, i, P, i, i, i, i, i, d, i, i,
+                                                 i, i, i, P, P, i, P, P]
+            lib.oracle_merge.argtypes = [P, P, i, i64, P, P]
             lib.oracle_mla_decode_split.argtypes = [P, P, P, P, i, d, d, d, P, i, P, i, i, i, i, i, d, i, i, i, i, i, P, P]
             lib.oracle_gather.argtypes = [P, P, i, P, i, P, i, i, i, P]
             lib.oracle_visibility_bits.argtypes = [P, i, i, i, i, i, P]
@@ -127,6 +133,45 @@ def decode(p: dict, rows=None, threads: int = 0):
     L = np.empty((n,), dtype=np.float64)
     lib.oracle_mla_decode(*args, rows_ptr, n, int(threads), _ptr(O), _ptr(L))
     del keep, rows_arr
+    return O, L
+
+
+def decode_ex(p: dict, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1, global_seq_lens=None,
+              local_visible_lens=None, threads: int = 0):
+    """The definition with decode context parallelism and per-token local bounds, all rows.
+
+    Under context parallelism (cp_world > 1) ``p`` holds one rank's share: its keys in
+    position order behind its own page table, ``seq_lens`` counting them, and
+    ``global_seq_lens`` [B] the whole sequences' lengths, on which the causal and window
+    bounds are taken.  ``local_visible_lens`` [B, Sq], when given, bounds each query
+    token's keys by local index (replacing the causal bound).  Returns (O, LSE) of
+    this share: merge the ranks' shares with ``merge``.
+    """
+    lib = _load()
+    keep, args, (B, Sq, H) = _common(p)
+    gsl = None if global_seq_lens is None else _i32(global_seq_lens)
+    lvl = None if local_visible_lens is None else _i32(local_visible_lens).reshape(B, Sq).copy()
+    n = B * Sq * H
+    O = np.empty((n, D_LATENT), dtype=np.float64)
+    L = np.empty((n,), dtype=np.float64)
+    rc = lib.oracle_mla_decode_ex(*args, int(cp_world), int(cp_rank), int(cp_interleave),
+                                  None if gsl is None else _ptr(gsl), None if lvl is None else _ptr(lvl),
+                                  int(threads), _ptr(O), _ptr(L))
+    if rc != 0:
+        raise ValueError("bad context-parallel arguments")
+    del keep, gsl, lvl
+    return O, L
+
+
+def merge(O_parts, L_parts):
+    """Combine per-rank (O [rows, 512], LSE [rows]) pieces over disjoint key sets."""
+    lib = _load()
+    Op = np.ascontiguousarray(np.stack([np.asarray(o, dtype=np.float64) for o in O_parts]))
+    Lp = np.ascontiguousarray(np.stack([np.asarray(x, dtype=np.float64) for x in L_parts]))
+    world, rows = Lp.shape
+    O = np.empty((rows, D_LATENT), dtype=np.float64)
+    L = np.empty((rows,), dtype=np.float64)
+    lib.oracle_merge(_ptr(Op), _ptr(Lp), int(world), int(rows), _ptr(O), _ptr(L))
     return O, L
 
 

@@ -22,7 +22,9 @@
  *                                          LSE = -inf, write_empty_output)
  *
  * Two routes compute it:
- *   oracle_mla_decode        the definition above, one row at a time;
+ *   oracle_mla_decode        the definition above, one row at a time
+ *                            (oracle_mla_decode_ex: the same with decode
+ *                            context parallelism and per-token local bounds);
  *   oracle_mla_decode_split  the pages' split-KV route: get_k_tile_count's
  *                            tile ranges, a normalized partial (O_i, lse_i)
  *                            per split, then reduction_kernel's base-2
@@ -120,6 +122,17 @@ typedef struct {
   int B, Sq, H, page_size, num_pages;
   double scale;
   int causal, window_left;
+  /* Decode context parallelism (kv_balanced_mla kernel page, __init__: cp_world,
+   * cp_rank, cp_interleave_size; __call__: causal_seqs).  The sequence's keys are
+   * dealt to cp_world ranks in runs of cp_interleave consecutive positions, run k
+   * to rank k % cp_world; this rank's cache holds its keys in position order and
+   * seq_lens counts them; global_seq_lens holds the whole sequence's length, which
+   * the causal and window bounds are taken on.  cp_world <= 1: no context parallelism. */
+  int cp_world, cp_rank, cp_interleave;
+  const int32_t *global_seq_lens; /* [B], or NULL without context parallelism */
+  /* __call__'s local_visible_lens: [B, Sq] exclusive bounds on the local key index,
+   * one per query token, replacing the causal bound when given (NULL: not given). */
+  const int32_t *local_visible_lens;
 } oracle_problem;
 
 /* Address of key j of request b: page_table[b][j / P], slot j % P. */
@@ -185,7 +198,8 @@ int oracle_mla_decode(const void *q_latent, const void *q_rope, const void *ckv,
                       double scale, int causal, int window_left, const int64_t *rows, int64_t n_rows,
                       int n_threads, double *O, double *LSE) {
   oracle_problem p = {q_latent, q_rope, ckv, kpe, dtype, q_descale, ckv_descale, kpe_descale, page_table,
-                      pt_stride, seq_lens, B, Sq, H, page_size, num_pages, scale, causal, window_left};
+                      pt_stride, seq_lens, B, Sq, H, page_size, num_pages, scale, causal, window_left,
+                      1, 0, 1, NULL, NULL};
   int64_t total = (int64_t)B * Sq * H;
   if (!rows) n_rows = total;
   int kmax = max_len(&p);
@@ -215,6 +229,138 @@ int oracle_mla_decode(const void *q_latent, const void *q_rope, const void *ckv,
 }
 
 /*
+ * Global position of local key l of this rank: the rank owns runs of cp_interleave
+ * consecutive positions, one run in every cycle of cp_world runs, so its local run
+ * l / I sits in cycle l / I at offset cp_rank * I within the cycle.
+ */
+static int64_t global_position(const oracle_problem *p, int64_t l) {
+  if (p->cp_world <= 1) return l;
+  int64_t I = p->cp_interleave, W = p->cp_world;
+  return (l / I) * W * I + (int64_t)p->cp_rank * I + l % I;
+}
+
+/*
+ * Is local key l of request b visible to query token t?  The causal and window
+ * bounds are the position rule of oracle_visible_range, taken on the global
+ * sequence (its length and the key's global position) under context parallelism;
+ * local_visible_lens, when given, replaces the causal bound with l < its entry.
+ */
+static int key_visible(const oracle_problem *p, int b, int t, int l) {
+  if (l < 0 || l >= p->seq_lens[b]) return 0;
+  int Kg = p->cp_world > 1 ? p->global_seq_lens[b] : p->seq_lens[b];
+  int lo, hi;
+  oracle_visible_range(Kg, p->Sq, t, p->causal, p->window_left, &lo, &hi);
+  int64_t g = global_position(p, l);
+  if (p->window_left >= 0 && g < lo) return 0;
+  if (p->local_visible_lens) return l < p->local_visible_lens[(int64_t)b * p->Sq + t];
+  if (p->causal) return g < hi;
+  return 1;
+}
+
+/*
+ * Softmax attention of row (b, t) over its visible keys, tested key by key:
+ * writes O[512] and returns the natural-log LSE (-inf and O = 0 when none).
+ */
+static double attend_visible(const oracle_problem *p, int b, int t, const double *ql, const double *qr, double *o,
+                             double *s_buf) {
+  int K = p->seq_lens[b];
+  for (int d = 0; d < ORACLE_DC; d++) o[d] = 0.0;
+  double m = -INFINITY;
+  int n = 0;
+  for (int j = 0; j < K; j++) {
+    if (!key_visible(p, b, t, j)) continue;
+    s_buf[j] = score(p, ql, qr, key_row(p, b, j));
+    if (s_buf[j] > m) m = s_buf[j];
+    n++;
+  }
+  if (n == 0) return -INFINITY;
+  double z = 0.0;
+  for (int j = 0; j < K; j++) {
+    if (!key_visible(p, b, t, j)) continue;
+    double w = exp(s_buf[j] - m);
+    int64_t row = key_row(p, b, j);
+    z += w;
+    for (int d = 0; d < ORACLE_DC; d++) o[d] += w * (load_elem(p->ckv, row * ORACLE_DC + d, p->dtype) * p->ckv_descale);
+  }
+  for (int d = 0; d < ORACLE_DC; d++) o[d] /= z;
+  return m + log(z);
+}
+
+/*
+ * The definition with context parallelism and local bounds: this rank's share
+ * of every row (its visible keys only), or the whole row when cp_world <= 1.
+ * Arguments as oracle_mla_decode, plus cp_world, cp_rank, cp_interleave,
+ * global_seq_lens [B] (may be NULL when cp_world <= 1) and local_visible_lens
+ * [B, Sq] (may be NULL).
+ */
+int oracle_mla_decode_ex(const void *q_latent, const void *q_rope, const void *ckv, const void *kpe, int dtype,
+                         double q_descale, double ckv_descale, double kpe_descale, const int32_t *page_table,
+                         int pt_stride, const int32_t *seq_lens, int B, int Sq, int H, int page_size, int num_pages,
+                         double scale, int causal, int window_left, int cp_world, int cp_rank, int cp_interleave,
+                         const int32_t *global_seq_lens, const int32_t *local_visible_lens, int n_threads, double *O,
+                         double *LSE) {
+  if (cp_world > 1 && (!global_seq_lens || cp_rank < 0 || cp_rank >= cp_world || cp_interleave < 1)) return 1;
+  oracle_problem p = {q_latent, q_rope, ckv, kpe, dtype, q_descale, ckv_descale, kpe_descale, page_table,
+                      pt_stride, seq_lens, B, Sq, H, page_size, num_pages, scale, causal, window_left,
+                      cp_world, cp_rank, cp_interleave, global_seq_lens, local_visible_lens};
+  int64_t total = (int64_t)B * Sq * H;
+  int kmax = max_len(&p);
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel
+#endif
+  {
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)kmax);
+    double ql[ORACLE_DC], qr[ORACLE_DR];
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < total; r++) {
+      int h = (int)(r % H);
+      int t = (int)((r / H) % Sq);
+      int b = (int)(r / ((int64_t)H * Sq));
+      load_query(&p, b, t, h, ql, qr);
+      LSE[r] = attend_visible(&p, b, t, ql, qr, O + r * ORACLE_DC, s_buf);
+    }
+    free(s_buf);
+  }
+  return 0;
+}
+
+/*
+ * Combine pieces of the same rows computed over disjoint key sets (the ranks of
+ * context parallelism): O_parts [world, rows, 512] normalized outputs and
+ * L_parts [world, rows] natural-log LSEs.  lse = m + ln(sum_r e^(L_r - m)) with m
+ * the largest L_r, O = sum_r e^(L_r - lse) O_r; pieces with L_r = -inf add
+ * nothing, and rows where every piece is empty get O = 0, lse = -inf.
+ */
+int oracle_merge(const double *O_parts, const double *L_parts, int world, int64_t rows, double *O, double *L) {
+  for (int64_t i = 0; i < rows; i++) {
+    double m = -INFINITY;
+    for (int r = 0; r < world; r++)
+      if (L_parts[(int64_t)r * rows + i] > m) m = L_parts[(int64_t)r * rows + i];
+    double *o = O + i * ORACLE_DC;
+    for (int d = 0; d < ORACLE_DC; d++) o[d] = 0.0;
+    if (m == -INFINITY) {
+      L[i] = -INFINITY;
+      continue;
+    }
+    double z = 0.0;
+    for (int r = 0; r < world; r++) z += exp(L_parts[(int64_t)r * rows + i] - m);
+    double lse = m + log(z);
+    for (int r = 0; r < world; r++) {
+      double lr = L_parts[(int64_t)r * rows + i];
+      if (lr == -INFINITY) continue;
+      double w = exp(lr - lse);
+      const double *src = O_parts + ((int64_t)r * rows + i) * ORACLE_DC;
+      for (int d = 0; d < ORACLE_DC; d++) o[d] += w * src[d];
+    }
+    L[i] = lse;
+  }
+  return 0;
+}
+
+/*
  * The split-KV route, following the page's planning and reduction steps:
  *
  * get_k_tile_count: with tile_n keys per tile,
@@ -239,7 +385,8 @@ int oracle_mla_decode_split(const void *q_latent, const void *q_rope, const void
                             int num_pages, double scale, int causal, int window_left, int split_kv, int tile_n,
                             int n_threads, double *O, double *LSE) {
   oracle_problem p = {q_latent, q_rope, ckv, kpe, dtype, q_descale, ckv_descale, kpe_descale, page_table,
-                      pt_stride, seq_lens, B, Sq, H, page_size, num_pages, scale, causal, window_left};
+                      pt_stride, seq_lens, B, Sq, H, page_size, num_pages, scale, causal, window_left,
+                      1, 0, 1, NULL, NULL};
   if (split_kv < 1 || tile_n < 1) return 1;
   int64_t total = (int64_t)B * Sq * H;
   int kmax = max_len(&p);

@@ -169,13 +169,15 @@ def _quantize_e4m3(x: torch.Tensor):
 
 
 def make_problem(w: Workload | str, *, seq_lens=None, seed=None, H=None, B=None, Sq=None, causal=None,
-                 window_left=None, dtype=None, out_dtype=None, pool_pages=None, table_width=None) -> Problem:
+                 window_left=None, dtype=None, out_dtype=None, pool_pages=None, table_width=None,
+                 page_size=None) -> Problem:
     """Draw one seeded decode batch.  Keyword overrides build smaller variants for tests."""
     if isinstance(w, str):
         w = WORKLOADS[w]
     over = {k: v for k, v in dict(seq_lens=seq_lens, seed=seed, H=H, B=B, Sq=Sq, causal=causal,
                                    window_left=window_left, dtype=dtype, out_dtype=out_dtype,
-                                   pool_pages=pool_pages, table_width=table_width).items() if v is not None}
+                                   pool_pages=pool_pages, table_width=table_width,
+                                   page_size=page_size).items() if v is not None}
     if over:
         d = dict(w.__dict__)
         d.update(over)
@@ -254,3 +256,52 @@ def sample_rows(prob: Problem, n: int, seed: int = 7) -> list:
     extra = torch.randint(0, total, (max(0, n - len(picks)),), generator=g).tolist()
     picks.update(extra)
     return sorted(picks)
+
+
+def dcp_owner(j: int, world: int, interleave: int) -> int:
+    """Rank holding key position j when positions are dealt in runs of `interleave` to the ranks in turn."""
+    return (j // interleave) % world
+
+
+def dcp_shard(prob: Problem, world: int, rank: int, interleave: int = 1, seed: int = 0) -> Problem:
+    """One rank's share of a batch under decode context parallelism (inputs only).
+
+    The rank holds the keys whose positions it owns (dcp_owner), in position order,
+    packed into its own pages behind its own page table; seq_lens counts them and
+    extra["global_seq_lens"] keeps the whole sequences' lengths.  Queries are the
+    same on every rank.  Cache slots past each local length are NaN poison.
+    """
+    P = prob.w.page_size
+    nan = _nan_bits(prob.ckv.dtype)
+    ibits = torch.int16 if prob.ckv.dtype == torch.bfloat16 else torch.uint8
+    src_c, src_k = prob.ckv.view(ibits).reshape(-1, D_LATENT), prob.kpe.view(ibits).reshape(-1, D_ROPE)
+    lens = prob.seq_lens.tolist()
+    local_rows, local_lens = [], []
+    for b, K in enumerate(lens):
+        mine = [j for j in range(K) if dcp_owner(j, world, interleave) == rank]
+        rows = [int(prob.page_table[b, j // P]) * P + j % P for j in mine]
+        local_rows.append(rows)
+        local_lens.append(len(rows))
+    n_pages = [(k + P - 1) // P for k in local_lens]
+    n_used = max(1, sum(n_pages))
+    width = max(1, max(n_pages))
+    ckv = torch.full((n_used * P, D_LATENT), nan, dtype=ibits)
+    kpe = torch.full((n_used * P, D_ROPE), nan, dtype=ibits)
+    table = torch.full((prob.B, width), PAD_PAGE, dtype=torch.int32)
+    cursor = 0
+    for b, rows in enumerate(local_rows):
+        if rows:
+            idx = torch.tensor(rows, dtype=torch.int64)
+            ckv[cursor * P: cursor * P + len(rows)] = src_c[idx]
+            kpe[cursor * P: cursor * P + len(rows)] = src_k[idx]
+        table[b, :n_pages[b]] = torch.arange(cursor, cursor + n_pages[b], dtype=torch.int32)
+        cursor += n_pages[b]
+    dt = prob.ckv.dtype
+    ckv = ckv.view(dt).reshape(n_used, P, D_LATENT)
+    kpe = kpe.view(dt).reshape(n_used, P, D_ROPE)
+    g = torch.Generator().manual_seed(seed * 7919 + rank)
+    phys = torch.randperm(n_used, generator=g).to(torch.int64)
+    return Problem(w=prob.w, q_latent=prob.q_latent, q_rope=prob.q_rope, ckv=ckv, kpe=kpe, page_table=table,
+                   seq_lens=torch.tensor(local_lens, dtype=torch.int32), phys_ids=phys, pool_pages=n_used,
+                   q_descale=prob.q_descale, ckv_descale=prob.ckv_descale, kpe_descale=prob.kpe_descale,
+                   extra={"global_seq_lens": prob.seq_lens.clone(), "cp": (world, rank, interleave)})

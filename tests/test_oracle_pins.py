@@ -96,6 +96,9 @@ CASES = [
     dict(lens=[129, 5], H=2, Sq=1, dtype=torch.float8_e4m3fn),
     dict(lens=[129, 70], H=2, Sq=2, causal=True, dtype=torch.float8_e4m3fn, descales=(0.03125, 0.0625, 0.5)),
     dict(lens=[40, 65], H=2, Sq=1, descales=(0.5, 2.0, 4.0)),
+    dict(lens=[100, 257, 16], H=2, Sq=2, causal=True, page_size=16),
+    dict(lens=[300, 129], H=2, Sq=3, causal=True, window_left=50, page_size=128),
+    dict(lens=[70, 9], H=2, Sq=1, page_size=8),
 ]
 
 
@@ -104,7 +107,7 @@ def test_matches_dense_sdpa(case):
     case = dict(case)
     p, starts = contiguous_problem(seed=11, **case)
     O, L = oracle.decode(p)
-    Oref, Lref = dense_reference(p, starts)
+    Oref, Lref = dense_reference(p, starts, page_size=case.get("page_size", 64))
     fin = np.isfinite(Lref)
     assert np.abs(O - Oref).max() <= 1e-12 * max(1.0, np.abs(Oref).max())
     assert np.all(np.abs(L[fin] - Lref[fin]) <= 1e-12 * np.maximum(1.0, np.abs(Lref[fin])))
@@ -310,3 +313,109 @@ def test_golden_two_key_example():
         assert abs(O[0, int(d)] - v) <= 1e-15
     assert O[0, 0] == pytest.approx(e / (e + 1), abs=1e-15)
     assert O[0, 1] == pytest.approx((2 * e - 4) / (e + 1), abs=1e-15)
+
+
+# ---------------------------------------------------------------- context parallelism and local bounds
+# Decode context parallelism splits every sequence's keys over ranks (runs of
+# cp_interleave_size positions dealt in turn, the kv_balanced_mla kernel page's
+# __init__ parameters); each rank attends to its own keys under the bounds of the
+# whole sequence (causal_seqs of __call__), and the ranks' (O, LSE) pieces combine
+# exactly.  The pin: the merged pieces equal the whole decode, so a wrong global
+# position, a wrong bound or a wrong combine fails.
+
+DCP_CASES = [
+    dict(world=2, interleave=1, lens=[100, 257, 1, 0, 64], Sq=1, causal=False, window=-1),
+    dict(world=2, interleave=1, lens=[300, 70, 5], Sq=3, causal=True, window=-1),
+    dict(world=3, interleave=2, lens=[300, 129, 2], Sq=4, causal=True, window=37),
+    dict(world=2, interleave=64, lens=[700, 64, 65], Sq=2, causal=True, window=-1),
+    dict(world=4, interleave=5, lens=[333, 17], Sq=2, causal=False, window=60),
+]
+
+
+@pytest.mark.parametrize("case", DCP_CASES, ids=lambda c: f"w{c['world']}i{c['interleave']}sq{c['Sq']}")
+def test_context_parallel_shares_merge_to_the_whole_decode(case):
+    prob = wl.make_problem("tiny", H=3, B=len(case["lens"]), seq_lens=case["lens"], Sq=case["Sq"],
+                           causal=case["causal"], window_left=case["window"], seed=17)
+    whole_O, whole_L = oracle.decode(prob.host_inputs())
+    Os, Ls = [], []
+    for r in range(case["world"]):
+        sh = wl.dcp_shard(prob, case["world"], r, case["interleave"])
+        O, L = oracle.decode_ex(sh.host_inputs(), cp_world=case["world"], cp_rank=r, cp_interleave=case["interleave"],
+                                global_seq_lens=sh.extra["global_seq_lens"])
+        Os.append(O)
+        Ls.append(L)
+    Om, Lm = oracle.merge(Os, Ls)
+    fin = np.isfinite(whole_L)
+    assert np.array_equal(np.isfinite(Lm), fin)
+    assert np.all(Om[~fin] == 0)
+    assert np.abs(Om - whole_O).max() <= 1e-12 * max(1.0, np.abs(whole_O).max())
+    assert np.abs(Lm[fin] - whole_L[fin]).max() <= 1e-12 * max(1.0, np.abs(whole_L[fin]).max())
+
+
+def test_one_rank_context_parallel_is_the_plain_decode():
+    prob = wl.make_problem("tiny", H=2, B=3, seq_lens=[90, 300, 3], Sq=3, causal=True, window_left=40, seed=3)
+    p = prob.host_inputs()
+    O1, L1 = oracle.decode(p)
+    O2, L2 = oracle.decode_ex(p, cp_world=1)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def test_merge_of_one_piece_and_an_empty_piece():
+    g = np.random.default_rng(1)
+    O = g.standard_normal((5, 512))
+    L = g.standard_normal(5)
+    Om, Lm = oracle.merge([O, np.zeros((5, 512))], [L, np.full(5, -np.inf)])
+    assert np.array_equal(Lm, L) and np.abs(Om - O).max() <= 1e-15
+    Om, Lm = oracle.merge([np.zeros((2, 512))] * 3, [np.full(2, -np.inf)] * 3)
+    assert np.all(Lm == -np.inf) and not Om.any()
+
+
+def dense_prefix_reference(p, starts, lvl, page_size=64):
+    """Library SDPA (fp64) with an explicit per-token prefix mask j < lvl[b, t] (and the window)."""
+    ql, qr = p["q_latent"].double(), p["q_rope"].double()
+    B, Sq, H, _ = ql.shape
+    ckv = p["ckv"].double().reshape(-1, 512)
+    kpe = p["kpe"].double().reshape(-1, 64)
+    outs, lses = [], []
+    for b in range(B):
+        K = int(p["seq_lens"][b])
+        base = starts[b] * page_size
+        c, k = ckv[base:base + K], kpe[base:base + K]
+        q = torch.cat([ql[b], qr[b]], dim=-1).permute(1, 0, 2)  # [H, Sq, 576]
+        keys = torch.cat([c, k], dim=-1)
+        j = torch.arange(K).unsqueeze(0)
+        mask = j < torch.as_tensor(lvl[b]).reshape(Sq, 1)
+        if p["window_left"] >= 0:
+            pos = torch.arange(Sq).unsqueeze(1) + (K - Sq)
+            mask &= j >= pos - p["window_left"]
+        s = (q @ keys.T) * p["scale"]
+        sm = s.masked_fill(~mask, -math.inf)
+        lse = torch.logsumexp(sm, dim=-1)
+        w = torch.where(mask, torch.exp(sm - torch.where(torch.isfinite(lse), lse, 0.0).unsqueeze(-1)), 0.0)
+        outs.append((w @ c).permute(1, 0, 2))
+        lses.append(lse.T)
+    return torch.stack(outs).reshape(-1, 512).numpy(), torch.stack(lses).reshape(-1).numpy()
+
+
+@pytest.mark.parametrize("window", [-1, 25])
+def test_local_visible_lens_match_dense_prefix_mask(window):
+    lens = [120, 260, 7]
+    p, starts = contiguous_problem(lens, H=2, Sq=3, seed=13, window_left=window)
+    lvl = [[0, 50, 120], [260, 3, 200], [7, 7, 1]]
+    O, L = oracle.decode_ex(p, local_visible_lens=lvl)
+    Oref, Lref = dense_prefix_reference(p, starts, lvl)
+    fin = np.isfinite(Lref)
+    assert np.array_equal(np.isfinite(L), fin)
+    assert np.all(O[~fin] == 0)
+    assert np.abs(O - Oref).max() <= 1e-12 * max(1.0, np.abs(Oref).max())
+    assert np.abs(L[fin] - Lref[fin]).max() <= 1e-12 * max(1.0, np.abs(Lref[fin]).max())
+
+
+def test_local_visible_lens_at_the_causal_bound_equal_causal():
+    lens = [90, 300, 3]
+    prob = wl.make_problem("tiny", H=2, B=3, seq_lens=lens, Sq=3, causal=True, seed=6)
+    p = prob.host_inputs()
+    lvl = [[K - (3 - 1 - t) for t in range(3)] for K in lens]
+    O1, L1 = oracle.decode(p)
+    O2, L2 = oracle.decode_ex(dict(p, causal=False), local_visible_lens=lvl)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
