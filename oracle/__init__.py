@@ -62,6 +62,7 @@ def _load():
             lib.oracle_mla_decode_split.argtypes = [P, P, P, P, i, d, d, d, P, i, P, i, i, i, i, i, d, i, i, i, i, i, P, P]
             lib.oracle_gather.argtypes = [P, P, i, P, i, P, i, i, i, P]
             lib.oracle_visibility_bits.argtypes = [P, i, i, i, i, i, P]
+            lib.oracle_visibility_bits_ex.argtypes = [P, i, i, i, i, i, i, i, P, P, i, P]
             lib.oracle_visible_range.argtypes = [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
             lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_f64.restype = d
@@ -208,6 +209,24 @@ def visibility_bits(seq_lens, Sq: int, causal: bool, window_left: int, max_k: in
     B = sl.shape[0]
     out = np.zeros((B, Sq, (max_k + 31) // 32), dtype=np.uint32)
     lib.oracle_visibility_bits(_ptr(sl), B, Sq, int(bool(causal)), int(window_left), max_k, _ptr(out))
+    return out
+
+
+def visibility_bits_ex(seq_lens, Sq: int, causal: bool, window_left: int, max_k: int, cp_world: int = 1,
+                       cp_rank: int = 0, cp_interleave: int = 1, global_seq_lens=None,
+                       local_visible_lens=None) -> np.ndarray:
+    """visibility_bits under decode context parallelism and local bounds (decode_ex's rule)."""
+    lib = _load()
+    sl = _i32(seq_lens)
+    B = sl.shape[0]
+    gsl = None if global_seq_lens is None else _i32(global_seq_lens)
+    lvl = None if local_visible_lens is None else _i32(local_visible_lens).reshape(B, Sq).copy()
+    out = np.zeros((B, Sq, (max_k + 31) // 32), dtype=np.uint32)
+    rc = lib.oracle_visibility_bits_ex(_ptr(sl), B, Sq, int(bool(causal)), int(window_left), int(cp_world),
+                                       int(cp_rank), int(cp_interleave), None if gsl is None else _ptr(gsl),
+                                       None if lvl is None else _ptr(lvl), max_k, _ptr(out))
+    if rc != 0:
+        raise ValueError("bad context-parallel arguments")
     return out
 
 

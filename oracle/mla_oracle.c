@@ -501,6 +501,38 @@ int oracle_visibility_bits(const int32_t *seq_lens, int B, int Sq, int causal, i
   return 0;
 }
 
+/*
+ * Visibility bits with context parallelism and local bounds: bit i of word w of
+ * row (b, t) is set iff local key 32*w + i passes key_visible (the rule of
+ * oracle_mla_decode_ex).  Arguments as there; bits [B, Sq, ceil(max_k / 32)].
+ */
+int oracle_visibility_bits_ex(const int32_t *seq_lens, int B, int Sq, int causal, int window_left, int cp_world,
+                              int cp_rank, int cp_interleave, const int32_t *global_seq_lens,
+                              const int32_t *local_visible_lens, int max_k, uint32_t *bits) {
+  if (cp_world > 1 && (!global_seq_lens || cp_rank < 0 || cp_rank >= cp_world || cp_interleave < 1)) return 1;
+  oracle_problem p;
+  memset(&p, 0, sizeof p);
+  p.seq_lens = seq_lens;
+  p.B = B;
+  p.Sq = Sq;
+  p.causal = causal;
+  p.window_left = window_left;
+  p.cp_world = cp_world;
+  p.cp_rank = cp_rank;
+  p.cp_interleave = cp_interleave;
+  p.global_seq_lens = global_seq_lens;
+  p.local_visible_lens = local_visible_lens;
+  int n_words = (max_k + 31) / 32;
+  for (int b = 0; b < B; b++)
+    for (int t = 0; t < Sq; t++) {
+      uint32_t *w = bits + ((int64_t)b * Sq + t) * n_words;
+      for (int i = 0; i < n_words; i++) w[i] = 0u;
+      for (int j = 0; j < max_k; j++)
+        if (key_visible(&p, b, t, j)) w[j / 32] |= 1u << (j % 32);
+    }
+  return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

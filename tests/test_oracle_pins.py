@@ -419,3 +419,31 @@ def test_local_visible_lens_at_the_causal_bound_equal_causal():
     O1, L1 = oracle.decode(p)
     O2, L2 = oracle.decode_ex(dict(p, causal=False), local_visible_lens=lvl)
     assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def test_visibility_bits_ex_plain_equals_position_rule():
+    lens = [0, 31, 32, 33, 100]
+    for Sq, causal, W in ((1, False, -1), (3, True, 7), (2, False, 5)):
+        assert np.array_equal(oracle.visibility_bits_ex(lens, Sq, causal, W, 128),
+                              oracle.visibility_bits(lens, Sq, causal, W, 128))
+
+
+@pytest.mark.parametrize("world,inter", [(2, 1), (3, 4), (4, 64)])
+def test_visibility_bits_ex_ranks_partition_the_global_bits(world, inter):
+    """Each rank's local bits, mapped to the positions it owns, are disjoint and together
+    equal the whole sequence's position-rule bits."""
+    glens = [0, 5, 130, 333]
+    Sq, causal, W, max_k = 3, True, 40, 400
+    whole = oracle.visibility_bits(glens, Sq, causal, W, max_k)
+    got = np.zeros_like(whole)
+    for r in range(world):
+        owned = [[j for j in range(K) if wl.dcp_owner(j, world, inter) == r] for K in glens]
+        bits = oracle.visibility_bits_ex([len(o) for o in owned], Sq, causal, W, max_k, cp_world=world, cp_rank=r,
+                                         cp_interleave=inter, global_seq_lens=glens)
+        for b, o in enumerate(owned):
+            for t in range(Sq):
+                for l, g in enumerate(o):
+                    if (int(bits[b, t, l // 32]) >> (l % 32)) & 1:
+                        assert not (int(got[b, t, g // 32]) >> (g % 32)) & 1
+                        got[b, t, g // 32] |= np.uint32(1 << (g % 32))
+    assert np.array_equal(got, whole)
