@@ -62,7 +62,8 @@ typedef enum {
 typedef enum { MLA_BF16 = 0, MLA_E4M3 = 1, MLA_F32 = 2 } mla_dtype_t;
 
 /*
- * Tensor metadata the decode call needs beyond its pointers.
+ * Tensor metadata the decode call needs beyond its pointers.  A zero-initialized
+ * struct with the first six fields and the descales set is a plain decode.
  *  seq_len_q          query tokens per request (1 = plain decode; >1 = speculative block)
  *  num_pages          pages in the cache pool (first dim of ckv / kpe)
  *  page_table_stride  int32 entries per request row of page_table (its second dim)
@@ -79,6 +80,34 @@ typedef enum { MLA_BF16 = 0, MLA_E4M3 = 1, MLA_F32 = 2 } mla_dtype_t;
  *                     created): when both are non-NULL, mla_decode records [0] just
  *                     before and [1] just after the split-KV kernel on the call's
  *                     stream, so the kernel can be timed alone; NULL: nothing recorded
+ *
+ * Decode context parallelism (the kv_balanced_mla kernel page: __init__'s cp_world,
+ * cp_rank, cp_interleave_size and __call__'s causal_seqs).  Every sequence's key
+ * positions are dealt to cp_world ranks in runs of cp_interleave consecutive
+ * positions, run k to rank k % cp_world.  Each rank's cache and page table hold its
+ * own keys in position order and its seq_lens count them; the causal and window
+ * bounds are taken on the whole sequence, whose lengths global_seq_lens gives.  Each
+ * rank's decode then yields its share (O, LSE) of every row, and mla_merge combines
+ * the ranks' shares into the whole decode.
+ *  cp_world           0 or 1: no context parallelism
+ *  cp_rank            this rank, 0 <= cp_rank < cp_world
+ *  cp_interleave      positions per run (0 is taken as 1)
+ *  global_seq_lens    device [B] int32, the whole sequences' lengths; required when
+ *                     cp_world > 1, ignored otherwise
+ *
+ *  local_visible_lens device [B, seq_len_q] int32 or NULL (__call__'s local_visible_lens):
+ *                     query token t of request b sees local keys below this bound (and
+ *                     above the window floor, when a window is set); it replaces the causal
+ *                     bound.  NULL: the causal flag decides.
+ *  partial_fp16       1: store the split pieces' normalized partial outputs as fp16
+ *                     (__init__'s partial_fp16) instead of fp32: half the reduction's
+ *                     bytes.  The partials hold O / l in units of the stored value codes,
+ *                     so every |ckv| code must stay within the fp16 range (always true for
+ *                     e4m3 codes, |x| <= 448; the caller's promise for bf16 caches).
+ *  reducer_d_tiles    CTAs per work row across the 512 output dims in the reduction:
+ *                     1, 2, 4 or 8 (0: 8)
+ *  use_pdl            1: launch the reduction with programmatic dependent launch, so its
+ *                     launch overlaps the split-KV kernel's end (not with split_timing)
  */
 typedef struct {
   int seq_len_q;
@@ -92,25 +121,40 @@ typedef struct {
   float kpe_descale;
   int num_clusters;
   void* split_timing[2];
+  int cp_world;
+  int cp_rank;
+  int cp_interleave;
+  const int32_t* global_seq_lens;
+  const int32_t* local_visible_lens;
+  int partial_fp16;
+  int reducer_d_tiles;
+  int use_pdl;
 } mla_config_t;
 
 /*
  * Plan a decode batch (host only; reads the host copy of seq_lens).
  *
- * The KV range of every (request, token) row is cut into tiles of 256 keys;
- * the visible tiles of all rows are laid end to end and dealt out in equal
- * contiguous shares to a persistent wave of clusters, so unequal lengths
- * balance (the page's get_split_kv / get_k_tile_count plan the same split per
- * request; this plan splits the whole batch at once).  Tiles wholly below a
- * sliding window are skipped.
+ * A request's seq_len_q * H (token, head) rows are cut into M tiles of 128 rows
+ * ("work rows"; consecutive tokens share a tile when H < 128, the page's pack_q).
+ * The KV range of every work row is cut into tiles of 256 keys; the visible
+ * tiles of all requests are laid end to end and dealt out in equal contiguous
+ * shares to a persistent wave of clusters, so unequal lengths balance (the page's
+ * get_split_kv / get_k_tile_count plan the same split per request; this plan splits
+ * the whole batch at once), with a request's work rows given to side-by-side
+ * clusters that read its KV together.  Tiles wholly outside every row's window are
+ * skipped.
  *
  *  seq_lens        host [B] int32, 0 <= seq_lens[b] <= page_table_stride * page_size
- *  B, H            requests and heads, 1 <= H <= 128
- *  page_size       keys per page: 64 (the only size the library supports)
+ *  B, H            requests and heads, 1 <= H <= 128, B * seq_len_q <= 16384
+ *  page_size       keys per page: a power of two from 8 to 1024
  *  window_left     -1 for full history, else >= 0
  *  cfg             tensor metadata as above
- *  split_kv        out: the most pieces any row is split into (1 = no reduction needed)
- *  workspace_bytes out: device workspace mla_decode needs for this batch
+ *  split_kv        out: the most pieces any work row is cut into (1 = no reduction
+ *                  needed); with context parallelism or local_visible_lens, whose
+ *                  device values the host does not see, an estimate that takes every
+ *                  local key as visible
+ *  workspace_bytes out: device workspace mla_decode needs; it depends on B, H,
+ *                  seq_len_q, the cluster count and partial_fp16 only, not on the lengths
  *
  * Returns MLA_ERR_CUDA when cfg->num_clusters == 0 and no device can be queried.
  */
@@ -137,6 +181,10 @@ MLA_API mla_status_t mla_plan(const int32_t *seq_lens, int B, int H, int page_si
  *
  * Cache slots past a request's length and pages no visible key uses may hold
  * any bits (NaN included) without affecting the result.
+ *
+ * Conditions only the device sees (a visible page id outside the pool, a device
+ * seq_lens value outside [0, page_table_stride * page_size], a bounded wait that
+ * gave up) do not change this return value: read them with mla_workspace_status.
  */
 MLA_API mla_status_t mla_decode(const void *q_latent, const void *q_rope, const void *ckv_cache, const void *kpe_cache,
                         const int32_t *page_table, const int32_t *seq_lens, float scale, int window_left, void *out,
@@ -176,6 +224,19 @@ MLA_API mla_status_t mla_decode_noalloc(const void *q_latent, const void *q_rope
 MLA_API mla_status_t mla_noalloc_status(cudaStream_t stream);
 
 /*
+ * Combine the ranks' shares of a context-parallel decode (see mla_config_t):
+ *  o_parts   [world, rows, 512] in dtype (MLA_F32 or MLA_BF16), rank r's output
+ *  lse_parts [world, rows] fp32 natural-log LSEs (-inf: the rank saw no visible key)
+ *  out       [rows, 512] in dtype;  lse [rows] fp32 or NULL
+ * lse = m + ln(sum_r e^(lse_r - m)), out = sum_r e^(lse_r - lse) o_r (the same combine
+ * as the split-KV reduction, reduction_kernel); rows with no visible key on any rank
+ * get out = 0 and lse = -inf.  rows = B * seq_len_q * H for a decode's outputs.  The
+ * exchange of the shares between ranks is the caller's (an all-gather).
+ */
+MLA_API mla_status_t mla_merge(const void *o_parts, const float *lse_parts, int world, long long rows,
+                               mla_dtype_t dtype, void *out, float *lse, cudaStream_t stream);
+
+/*
  * Debug gather: the decode kernel's page walk and tile load, written back densely.
  *  dense_out [B, max_k, 576] elements of qkv_dtype: row j of request b is
  *  (c_j | kpe_j) for j < seq_lens[b] and zero bytes for j >= seq_lens[b].
@@ -186,7 +247,8 @@ MLA_API mla_status_t mla_debug_gather(const void *ckv_cache, const void *kpe_cac
                               void *dense_out, cudaStream_t stream);
 
 /*
- * Debug mask: the decode kernel's visibility rule, one bit per key.
+ * Debug mask: the decode kernel's visibility rule, one bit per key (with the
+ * context-parallel lengths and local bounds of cfg when set).
  *  bits [B, seq_len_q, ceil(max_k/32)] uint32: bit i of word w is set iff key
  *  32*w + i is visible to that (request, token) row.
  */
@@ -211,9 +273,8 @@ MLA_API mla_status_t mla_debug_wait_timeout(unsigned timeout_us, uint32_t *statu
  *   MLA_OK               nothing went wrong on the device
  *   MLA_ERR_TIMEOUT      a bounded device wait gave up (the kernel unwound instead of hanging)
  *   MLA_ERR_INVALID_ARG  a visible page-table entry outside [0, num_pages) (read as zeros),
- *                        a device seq_lens value outside [0, page_table_stride * page_size),
- *                        or a batch that gave one cluster more pieces than it can hold
- *                        (a batch that mla_plan rejected with MLA_ERR_UNSUPPORTED)
+ *                        or a device seq_lens value outside [0, page_table_stride * page_size)
+ *                        (clamped into it)
  * mla_decode cannot see these conditions (it returns once the kernels are
  * enqueued); the output of a call that reports one is incomplete.  Not for the
  * decode path.

@@ -6,4 +6,4 @@ draws seeded synthetic decode batches.
 """
 
 from . import workloads  # noqa: F401
-from .api import PagedMlaDecoder, decoder_for  # noqa: F401
+from .api import PagedMlaDecoder, decoder_for, merge_ranks  # noqa: F401

@@ -20,8 +20,8 @@ MLA_BF16, MLA_E4M3, MLA_F32 = 0, 1, 2
 
 _DTYPES = {torch.bfloat16: MLA_BF16, torch.float8_e4m3fn: MLA_E4M3, torch.float32: MLA_F32}
 
-EXPORTS = ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_noalloc_status", "mla_debug_gather", "mla_debug_mask",
-           "mla_debug_wait_timeout", "mla_workspace_status", "mla_status_string")
+EXPORTS = ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_noalloc_status", "mla_merge", "mla_debug_gather",
+           "mla_debug_mask", "mla_debug_wait_timeout", "mla_workspace_status", "mla_status_string")
 
 
 class MlaError(RuntimeError):
@@ -43,6 +43,14 @@ class MlaConfig(ctypes.Structure):
         ("kpe_descale", ctypes.c_float),
         ("num_clusters", ctypes.c_int),
         ("split_timing", ctypes.c_void_p * 2),
+        ("cp_world", ctypes.c_int),
+        ("cp_rank", ctypes.c_int),
+        ("cp_interleave", ctypes.c_int),
+        ("global_seq_lens", ctypes.c_void_p),
+        ("local_visible_lens", ctypes.c_void_p),
+        ("partial_fp16", ctypes.c_int),
+        ("reducer_d_tiles", ctypes.c_int),
+        ("use_pdl", ctypes.c_int),
     ]
 
 
@@ -73,10 +81,11 @@ def load(path: str | None = None):
             lib.mla_debug_wait_timeout.argtypes = [ctypes.c_uint, P, P]
             lib.mla_workspace_status.argtypes = [P, S, P]
             lib.mla_noalloc_status.argtypes = [P]
+            lib.mla_merge.argtypes = [P, P, I, ctypes.c_longlong, I, P, P, P]
             lib.mla_status_string.argtypes = [I]
             lib.mla_status_string.restype = ctypes.c_char_p
-            for fn in ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_noalloc_status", "mla_debug_gather",
-                       "mla_debug_mask", "mla_debug_wait_timeout", "mla_workspace_status"):
+            for fn in ("mla_plan", "mla_decode", "mla_decode_noalloc", "mla_noalloc_status", "mla_merge",
+                       "mla_debug_gather", "mla_debug_mask", "mla_debug_wait_timeout", "mla_workspace_status"):
                 getattr(lib, fn).restype = I
             _lib = lib
     return _lib
@@ -103,11 +112,23 @@ def _stream(stream):
 
 def make_config(*, seq_len_q: int, num_pages: int, page_table_stride: int, qkv_dtype, out_dtype=torch.bfloat16,
                 causal: bool = False, q_descale: float = 1.0, ckv_descale: float = 1.0, kpe_descale: float = 1.0,
-                num_clusters: int = 0) -> MlaConfig:
+                num_clusters: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1,
+                partial_fp16: bool = False, reducer_d_tiles: int = 0, use_pdl: bool = False) -> MlaConfig:
+    """The C config; the device pointers global_seq_lens / local_visible_lens are set per call
+    (set_call_inputs), since their tensors belong to the call."""
     qd = _DTYPES[qkv_dtype] if isinstance(qkv_dtype, torch.dtype) else int(qkv_dtype)
     od = _DTYPES[out_dtype] if isinstance(out_dtype, torch.dtype) else int(out_dtype)
-    return MlaConfig(int(seq_len_q), int(num_pages), int(page_table_stride), qd, od, int(bool(causal)),
-                     float(q_descale), float(ckv_descale), float(kpe_descale), int(num_clusters))
+    c = MlaConfig(int(seq_len_q), int(num_pages), int(page_table_stride), qd, od, int(bool(causal)),
+                  float(q_descale), float(ckv_descale), float(kpe_descale), int(num_clusters))
+    c.cp_world, c.cp_rank, c.cp_interleave = int(cp_world), int(cp_rank), int(cp_interleave)
+    c.partial_fp16, c.reducer_d_tiles, c.use_pdl = int(bool(partial_fp16)), int(reducer_d_tiles), int(bool(use_pdl))
+    return c
+
+
+def set_call_inputs(cfg: MlaConfig, global_seq_lens=None, local_visible_lens=None):
+    """Point the config at this call's device tensors (or clear them)."""
+    cfg.global_seq_lens = None if global_seq_lens is None else global_seq_lens.data_ptr()
+    cfg.local_visible_lens = None if local_visible_lens is None else local_visible_lens.data_ptr()
 
 
 def mla_plan(seq_lens, B: int, H: int, page_size: int, window_left: int, cfg: MlaConfig):
@@ -138,6 +159,14 @@ def mla_decode_noalloc(q_latent, q_rope, ckv_cache, kpe_cache, page_table, seq_l
         _ptr(q_latent), _ptr(q_rope), _ptr(ckv_cache), _ptr(kpe_cache), _ptr(page_table), _ptr(seq_lens),
         float(scale), int(window_left), _ptr(out), _ptr(lse), _stream(stream), int(B), int(H),
         int(ckv_cache.shape[1]), ctypes.byref(cfg)))
+
+
+def mla_merge(o_parts, lse_parts, out, lse=None, stream=None):
+    """Combine per-rank shares: o_parts [world, rows, 512] (fp32 or bf16), lse_parts [world, rows] fp32."""
+    world = o_parts.shape[0]
+    rows = o_parts.numel() // (world * 512)
+    _check("mla_merge", load().mla_merge(_ptr(o_parts), _ptr(lse_parts), int(world), int(rows),
+                                         _DTYPES[o_parts.dtype], _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def mla_noalloc_status(stream=None) -> int:

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -24,9 +26,11 @@ namespace {
 
 constexpr int kMaxRows = 16384;   // B * seq_len_q (schedule scratch in shared memory)
 constexpr int kMaxSeqLenQ = 64;
-constexpr int kMaxSegments = 256;  // pieces one cluster may own (the split-KV kernel's segment list)
+constexpr int kMaxWorld = 1024;
+constexpr int kMaxClusters = 1024;  // the partial slot of a segment has 18 bits
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 mla_status_t validate_cfg(const mla_config_t* cfg, int B, int H, int page_size, int window_left) {
   if (!cfg) return MLA_ERR_INVALID_ARG;
@@ -41,11 +45,26 @@ mla_status_t validate_cfg(const mla_config_t* cfg, int B, int H, int page_size, 
     return MLA_ERR_INVALID_ARG;
   // one scale for the whole key (latent and rope parts are one contraction)
   if (cfg->qkv_dtype == MLA_E4M3 && cfg->ckv_descale != cfg->kpe_descale) return MLA_ERR_UNSUPPORTED;
-  if (H > kMaxHeads || page_size != kPageSize || cfg->seq_len_q > kMaxSeqLenQ) return MLA_ERR_UNSUPPORTED;
+  if (page_size < 1) return MLA_ERR_INVALID_ARG;
+  if (!pow2(page_size) || page_size < kMinPageSize || page_size > kMaxPageSize) return MLA_ERR_UNSUPPORTED;
+  if (H > kMaxHeads || cfg->seq_len_q > kMaxSeqLenQ) return MLA_ERR_UNSUPPORTED;
   if ((long long)B * cfg->seq_len_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
-  if ((long long)cfg->page_table_stride * kPageSize > (1ll << 30)) return MLA_ERR_UNSUPPORTED;
+  if (cfg->num_clusters > kMaxClusters) return MLA_ERR_UNSUPPORTED;
+  if ((long long)cfg->page_table_stride * page_size > (1ll << 30)) return MLA_ERR_UNSUPPORTED;
+  if (cfg->cp_world < 0 || cfg->cp_interleave < 0) return MLA_ERR_INVALID_ARG;
+  if (cfg->cp_world > 1) {
+    if (cfg->cp_world > kMaxWorld || cfg->cp_rank < 0 || cfg->cp_rank >= cfg->cp_world) return MLA_ERR_INVALID_ARG;
+  }
+  if (cfg->partial_fp16 != 0 && cfg->partial_fp16 != 1) return MLA_ERR_INVALID_ARG;
+  if (cfg->reducer_d_tiles != 0 && cfg->reducer_d_tiles != 1 && cfg->reducer_d_tiles != 2 &&
+      cfg->reducer_d_tiles != 4 && cfg->reducer_d_tiles != 8)
+    return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
+
+int cp_world_of(const mla_config_t* cfg) { return cfg->cp_world > 1 ? cfg->cp_world : 1; }
+int cp_interleave_of(const mla_config_t* cfg) { return cfg->cp_interleave > 0 ? cfg->cp_interleave : 1; }
+int d_tiles_of(const mla_config_t* cfg) { return cfg->reducer_d_tiles > 0 ? cfg->reducer_d_tiles : 8; }
 
 // clusters of one persistent wave on the current device (cached per device)
 int resolve_clusters(const mla_config_t* cfg, bool e4m3, int* out) {
@@ -65,42 +84,52 @@ int resolve_clusters(const mla_config_t* cfg, bool e4m3, int* out) {
   return 0;
 }
 
-struct HostPlan {
-  int R, G, T, max_parts, max_segments;
-};
-
-// Host mirror of the device schedule (same functions, same integer arithmetic).
-HostPlan plan_rows(const int32_t* seq_lens, int B, int Sq, int causal, int window_left, int stride, int G) {
-  HostPlan hp{};
-  hp.R = B * Sq;
-  hp.G = G;
-  std::vector<long long> prefix(hp.R + 1, 0);
-  std::vector<int> n(hp.R, 0);
-  for (int r = 0; r < hp.R; ++r) {
-    int K = seq_lens[r / Sq];
-    K = K < 0 ? 0 : (K > stride * kPageSize ? stride * kPageSize : K);
-    int lo, hi, tlo, nt;
-    visible_range(K, Sq, r % Sq, causal, window_left, lo, hi);
-    tile_span(lo, hi, tlo, nt);
-    n[r] = nt;
-    prefix[r + 1] = prefix[r] + (nt > 0 ? nt + kPieceCost : 0);
+// Host mirror of the device deal (same functions, same integer arithmetic) over host
+// lengths: the most pieces any work row is cut into.  Under context parallelism or with
+// local bounds (whose device values the host does not have) every local key is taken
+// as visible, which makes the count an estimate.
+int plan_max_parts(const int32_t* seq_lens, int B, int H, int page_size, int window_left, const mla_config_t* cfg,
+                   int G) {
+  const int Sq = cfg->seq_len_q;
+  const DealShape d = deal_shape(B, Sq, H, G);
+  const bool exact = cp_world_of(cfg) == 1 && !cfg->local_visible_lens;
+  auto span = [&](int b, int t0, int t1, int& tlo, int& n) {
+    int K = seq_lens[b];
+    K = K < 0 ? 0 : (K > cfg->page_table_stride * page_size ? cfg->page_table_stride * page_size : K);
+    int lo_min = INT_MAX, hi_max = 0;
+    for (int t = t0; t <= t1; ++t) {
+      int lo = 0, hi = K;
+      if (exact) token_range(K, K, 0, false, Sq, t, cfg->causal, window_left, 1, 0, 1, lo, hi);
+      if (hi > lo) {
+        lo_min = std::min(lo_min, lo);
+        hi_max = std::max(hi_max, hi);
+      }
+    }
+    if (hi_max > 0) tile_span(lo_min, hi_max, tlo, n);
+    else tlo = n = 0;
+  };
+  std::vector<long long> prefix(d.S + 1, 0);
+  std::vector<int> ulo(d.S), U(d.S);
+  for (int s = 0; s < d.S; ++s) {
+    const int b = s / d.nsub, k = s % d.nsub;
+    int t0, t1;
+    work_tokens(k * d.wb, std::min(d.Qb, k * d.wb + d.wb) - 1, Sq, H, t0, t1);
+    span(b, t0, t1, ulo[s], U[s]);
+    prefix[s + 1] = prefix[s] + (U[s] > 0 ? U[s] + kPieceCost : 0);
   }
-  const long long T = prefix[hp.R];
-  hp.T = (int)T;
-  hp.max_parts = 0;
-  G = deal_clusters(G, T);
-  std::vector<int> segs(G, 0);
-  for (int r = 0; r < hp.R; ++r) {
-    if (n[r] == 0) continue;
-    const long long pb = prefix[r] + kPieceCost;
-    const int cf = cluster_of_tile(pb, T, G), cl = cluster_of_tile(pb + n[r] - 1, T, G);
-    if (cl - cf + 1 > hp.max_parts) hp.max_parts = cl - cf + 1;
-    for (int c = cf; c <= cl; ++c) segs[c]++;
+  const long long T = prefix[d.S];
+  const int Gd = deal_groups(d.Gg, T);
+  int most = 1;
+  for (int w = 0; w < d.Rw; ++w) {
+    const int b = w / d.Qb, i = w % d.Qb, s = b * d.nsub + i / d.wb;
+    int t0, t1, tlo, n;
+    work_tokens(i, i, Sq, H, t0, t1);
+    span(b, t0, t1, tlo, n);
+    if (n <= 0) continue;
+    const long long xf = prefix[s] + kPieceCost + (tlo - ulo[s]);
+    most = std::max(most, group_of_tile(xf + n - 1, T, Gd) - group_of_tile(xf, T, Gd) + 1);
   }
-  hp.max_segments = 0;
-  for (int c = 0; c < G; ++c)
-    if (segs[c] > hp.max_segments) hp.max_segments = segs[c];
-  return hp;
+  return most;
 }
 
 // ------------------------------------------------------------------ TMA descriptors
@@ -133,19 +162,64 @@ bool encode3d(CUtensorMap* m, const void* base, bool e4m3, uint64_t d0, uint64_t
   return r == CUDA_SUCCESS;
 }
 
+// KV maps: [pages][P][D] with boxes of one page's box_rows(P) rows; Q maps: [B][Sq * H][D]
+// with boxes of 64 (token, head) rows (a work row's rows past Sq * H read as zeros).
 bool encode_kv_maps(KvMaps* maps, const void* ckv, const void* kpe, const void* q_latent, const void* q_rope, bool e4m3,
-                    int num_pages, int rows_q, int H) {
+                    int num_pages, int page_size, int B, int rows_q) {
   const uint32_t blk = e4m3 ? 128 : 64;
   const CUtensorMapSwizzle rope_sw = e4m3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint32_t br = (uint32_t)box_rows(page_size);
   memset(maps, 0, sizeof(*maps));
-  bool ok = encode3d(&maps->ckv, ckv, e4m3, kDLatent, kPageSize, (uint64_t)num_pages, blk, kPageSize,
+  bool ok = encode3d(&maps->ckv, ckv, e4m3, kDLatent, (uint64_t)page_size, (uint64_t)num_pages, blk, br,
                      CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode3d(&maps->kpe, kpe, e4m3, kDRope, kPageSize, (uint64_t)num_pages, kDRope, kPageSize, rope_sw);
+            encode3d(&maps->kpe, kpe, e4m3, kDRope, (uint64_t)page_size, (uint64_t)num_pages, kDRope, br, rope_sw);
   if (ok && q_latent)
-    ok = encode3d(&maps->q_latent, q_latent, e4m3, kDLatent, (uint64_t)H, (uint64_t)rows_q, blk, kRowsPerCta,
+    ok = encode3d(&maps->q_latent, q_latent, e4m3, kDLatent, (uint64_t)rows_q, (uint64_t)B, blk, kRowsPerCta,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode3d(&maps->q_rope, q_rope, e4m3, kDRope, (uint64_t)H, (uint64_t)rows_q, kDRope, kRowsPerCta, rope_sw);
+         encode3d(&maps->q_rope, q_rope, e4m3, kDRope, (uint64_t)rows_q, (uint64_t)B, kDRope, kRowsPerCta, rope_sw);
   return ok;
+}
+
+// decode parameters from the call's arguments (validated)
+DecodeParams make_params(const void* q_latent, const void* q_rope, const void* ckv_cache, const void* kpe_cache,
+                         const int32_t* page_table, const int32_t* seq_lens, float scale, int window_left, void* out,
+                         float* lse, void* workspace, int B, int H, int page_size, const mla_config_t* cfg, int G) {
+  DecodeParams p{};
+  p.q_latent = q_latent;
+  p.q_rope = q_rope;
+  p.ckv = ckv_cache;
+  p.kpe = kpe_cache;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.global_seq_lens = cp_world_of(cfg) > 1 ? cfg->global_seq_lens : nullptr;
+  p.local_visible_lens = cfg->local_visible_lens;
+  p.out = out;
+  p.lse = lse;
+  p.ws = static_cast<uint8_t*>(workspace);
+  p.B = B;
+  p.Sq = cfg->seq_len_q;
+  p.H = H;
+  p.num_pages = cfg->num_pages;
+  p.pt_stride = cfg->page_table_stride;
+  p.page_size = page_size;
+  p.page_shift = 0;
+  while ((1 << p.page_shift) < page_size) ++p.page_shift;
+  p.causal = cfg->causal ? 1 : 0;
+  p.window_left = window_left;
+  p.cp_world = cp_world_of(cfg);
+  p.cp_rank = p.cp_world > 1 ? cfg->cp_rank : 0;
+  p.cp_interleave = cp_interleave_of(cfg);
+  p.qkv_e4m3 = cfg->qkv_dtype == MLA_E4M3 ? 1 : 0;
+  p.out_f32 = cfg->out_dtype == MLA_F32 ? 1 : 0;
+  p.partial_f16 = cfg->partial_fp16 ? 1 : 0;
+  p.num_clusters = G;
+  p.reduce_d_tiles = d_tiles_of(cfg);
+  p.scale = scale;
+  p.q_descale = cfg->q_descale;
+  p.ckv_descale = cfg->ckv_descale;
+  p.kpe_descale = cfg->kpe_descale;
+  p.score_scale_log2 = scale * cfg->q_descale * cfg->ckv_descale * 1.4426950408889634f;
+  return p;
 }
 
 mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
@@ -172,14 +246,12 @@ mla_status_t mla_plan(const int32_t* seq_lens, int B, int H, int page_size, int 
   mla_status_t st = validate_cfg(cfg, B, H, page_size, window_left);
   if (st != MLA_OK) return st;
   for (int b = 0; b < B; ++b)
-    if (seq_lens[b] < 0 || (long long)seq_lens[b] > (long long)cfg->page_table_stride * kPageSize)
+    if (seq_lens[b] < 0 || (long long)seq_lens[b] > (long long)cfg->page_table_stride * page_size)
       return MLA_ERR_INVALID_ARG;
   int G;
   if (resolve_clusters(cfg, cfg->qkv_dtype == MLA_E4M3, &G) != 0) return MLA_ERR_CUDA;
-  HostPlan hp = plan_rows(seq_lens, B, cfg->seq_len_q, cfg->causal, window_left, cfg->page_table_stride, G);
-  if (hp.max_segments > kMaxSegments) return MLA_ERR_UNSUPPORTED;
-  *split_kv = hp.max_parts < 1 ? 1 : hp.max_parts;
-  *workspace_bytes = ws_layout(hp.R, G).total;
+  *split_kv = plan_max_parts(seq_lens, B, H, page_size, window_left, cfg, G);
+  *workspace_bytes = ws_layout(B, cfg->seq_len_q, H, G, cfg->partial_fp16 ? 1 : 0).total;
   return MLA_OK;
 }
 
@@ -191,6 +263,7 @@ mla_status_t mla_decode(const void* q_latent, const void* q_rope, const void* ck
   if (st != MLA_OK) return st;
   if (!q_latent || !q_rope || !ckv_cache || !kpe_cache || !page_table || !seq_lens || !out || !workspace)
     return MLA_ERR_INVALID_ARG;
+  if (cp_world_of(cfg) > 1 && !cfg->global_seq_lens) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q_latent) || !aligned16(q_rope) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
       !aligned16(page_table) || !aligned16(seq_lens) || !aligned16(out) || (lse && !aligned16(lse)) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -199,37 +272,15 @@ mla_status_t mla_decode(const void* q_latent, const void* q_rope, const void* ck
   const bool e4m3 = cfg->qkv_dtype == MLA_E4M3;
   int G;
   if (resolve_clusters(cfg, e4m3, &G) != 0) return MLA_ERR_CUDA;
-  const int R = B * cfg->seq_len_q;
-  if (workspace_bytes < ws_layout(R, G).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < ws_layout(B, cfg->seq_len_q, H, G, cfg->partial_fp16 ? 1 : 0).total)
+    return MLA_ERR_WORKSPACE_TOO_SMALL;
 
-  DecodeParams p{};
-  p.q_latent = q_latent;
-  p.q_rope = q_rope;
-  p.ckv = ckv_cache;
-  p.kpe = kpe_cache;
-  p.page_table = page_table;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.lse = lse;
-  p.ws = static_cast<uint8_t*>(workspace);
-  p.B = B;
-  p.Sq = cfg->seq_len_q;
-  p.H = H;
-  p.num_pages = cfg->num_pages;
-  p.pt_stride = cfg->page_table_stride;
-  p.causal = cfg->causal ? 1 : 0;
-  p.window_left = window_left;
-  p.qkv_e4m3 = e4m3 ? 1 : 0;
-  p.out_f32 = cfg->out_dtype == MLA_F32 ? 1 : 0;
-  p.num_clusters = G;
-  p.scale = scale;
-  p.q_descale = cfg->q_descale;
-  p.ckv_descale = cfg->ckv_descale;
-  p.kpe_descale = cfg->kpe_descale;
-  p.score_scale_log2 = scale * cfg->q_descale * cfg->ckv_descale * 1.4426950408889634f;
-
+  const DecodeParams p = make_params(q_latent, q_rope, ckv_cache, kpe_cache, page_table, seq_lens, scale, window_left,
+                                     out, lse, workspace, B, H, page_size, cfg, G);
   KvMaps maps;
-  if (!encode_kv_maps(&maps, ckv_cache, kpe_cache, q_latent, q_rope, e4m3, cfg->num_pages, R, H)) return MLA_ERR_CUDA;
+  if (!encode_kv_maps(&maps, ckv_cache, kpe_cache, q_latent, q_rope, e4m3, cfg->num_pages, page_size, B,
+                      cfg->seq_len_q * H))
+    return MLA_ERR_CUDA;
   const bool timed = cfg->split_timing[0] && cfg->split_timing[1];
   if (timed && cudaEventRecord(static_cast<cudaEvent_t>(cfg->split_timing[0]), stream) != cudaSuccess)
     return MLA_ERR_CUDA;
@@ -237,7 +288,19 @@ mla_status_t mla_decode(const void* q_latent, const void* q_rope, const void* ck
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (timed && cudaEventRecord(static_cast<cudaEvent_t>(cfg->split_timing[1]), stream) != cudaSuccess)
     return MLA_ERR_CUDA;
-  return cuda_status(launch_reduce(p, stream));
+  // the PDL reduction starts its launch while the split-KV kernel drains; it is not used
+  // when the split kernel is timed alone (its end event would then come late)
+  return cuda_status(launch_reduce(p, stream, cfg->use_pdl != 0 && !timed));
+}
+
+mla_status_t mla_merge(const void* o_parts, const float* lse_parts, int world, long long rows, mla_dtype_t dtype,
+                       void* out, float* lse, cudaStream_t stream) {
+  if (!o_parts || !lse_parts || !out || world < 1 || world > kMaxWorld || rows < 1) return MLA_ERR_INVALID_ARG;
+  if (dtype != MLA_F32 && dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_merge(o_parts, lse_parts, world, rows, dtype == MLA_F32 ? 1 : 0, out, lse, stream));
 }
 
 mla_status_t mla_debug_gather(const void* ckv_cache, const void* kpe_cache, const int32_t* page_table,
@@ -249,19 +312,21 @@ mla_status_t mla_debug_gather(const void* ckv_cache, const void* kpe_cache, cons
   if (!aligned16(ckv_cache) || !aligned16(kpe_cache) || !aligned16(dense_out)) return MLA_ERR_INVALID_ARG;
   const bool e4m3 = cfg->qkv_dtype == MLA_E4M3;
   KvMaps maps;
-  if (!encode_kv_maps(&maps, ckv_cache, kpe_cache, nullptr, nullptr, e4m3, cfg->num_pages, 1, 1))
+  if (!encode_kv_maps(&maps, ckv_cache, kpe_cache, nullptr, nullptr, e4m3, cfg->num_pages, page_size, 1, 1))
     return MLA_ERR_CUDA;
   return cuda_status(launch_debug_gather(maps, e4m3, page_table, seq_lens, B, cfg->page_table_stride, cfg->num_pages,
-                                         max_k, dense_out, nullptr, stream));
+                                         page_size, max_k, dense_out, nullptr, stream));
 }
 
 mla_status_t mla_debug_mask(const int32_t* seq_lens, int B, int window_left, int max_k, const mla_config_t* cfg,
                             uint32_t* bits, cudaStream_t stream) {
-  mla_status_t st = validate_cfg(cfg, B, 1, kPageSize, window_left);
+  mla_status_t st = validate_cfg(cfg, B, 1, kKeyGroup, window_left);
   if (st != MLA_OK) return st;
   if (!seq_lens || !bits || max_k < 1) return MLA_ERR_INVALID_ARG;
-  return cuda_status(
-      launch_debug_mask(seq_lens, B, cfg->seq_len_q, cfg->causal ? 1 : 0, window_left, max_k, bits, stream));
+  if (cp_world_of(cfg) > 1 && !cfg->global_seq_lens) return MLA_ERR_INVALID_ARG;
+  const DecodeParams p = make_params(nullptr, nullptr, nullptr, nullptr, nullptr, seq_lens, 1.f, window_left, nullptr,
+                                     nullptr, nullptr, B, 1, kKeyGroup, cfg, 1);
+  return cuda_status(launch_debug_mask(p, max_k, bits, stream));
 }
 
 mla_status_t mla_debug_wait_timeout(unsigned timeout_us, uint32_t* status_words, cudaStream_t stream) {
@@ -279,10 +344,11 @@ mla_status_t mla_workspace_status(const void* workspace, size_t workspace_bytes,
   WsHeader h;
   if (cudaMemcpy(&h, workspace, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
   if (h.num_clusters <= 0 || h.num_rows <= 0) return MLA_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(h.num_rows, h.num_clusters);
-  if (workspace_bytes < L.total) return MLA_ERR_INVALID_ARG;
+  // the status words follow the header (the start of every workspace layout)
+  const size_t off = align256(sizeof(WsHeader));
+  if (workspace_bytes < off + 8 * (size_t)h.num_clusters) return MLA_ERR_INVALID_ARG;
   std::vector<uint32_t> words(2 * (size_t)h.num_clusters);
-  if (cudaMemcpy(words.data(), static_cast<const uint8_t*>(workspace) + L.cta_status, words.size() * 4,
+  if (cudaMemcpy(words.data(), static_cast<const uint8_t*>(workspace) + off, words.size() * 4,
                  cudaMemcpyDeviceToHost) != cudaSuccess)
     return MLA_ERR_CUDA;
   uint32_t all = 0;

@@ -1,10 +1,14 @@
-// Split-KV reduction and the debug kernels (gather, mask).
+// Split-KV reduction, the context-parallel merge and the debug kernels (gather, mask).
 //
 // The reduction follows reduction_kernel of the kv_balanced_mla kernel page:
 // the global base-2 log-sum-exp of a row's pieces is lse = max + log2(sum
 // 2^(lse_i - max)) (max taken as 0 when every piece is empty), and the output
-// is sum_i 2^(lse_i - lse) * O_i over the row's normalized partials.
+// is output_scale * sum_i 2^(lse_i - lse) * O_i over the row's normalized
+// partials (fp32, or fp16 as __init__'s partial_fp16 allows: a normalized partial
+// is a convex combination of stored value codes), in 1, 2, 4 or 8 bands of the 512
+// output dims (reducer_d_tiles).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "mla_common.cuh"
@@ -15,104 +19,214 @@
 
 namespace mla {
 
-// One CTA per (row, 64 dims): the row's pieces combined with weights
-// exp2(lse_i - lse), lse = log2 of the summed exp2(lse_i) (one piece: weight 1, a
-// copy).  Pieces are workspace slots laid out [dim / 4][head][dim % 4], so a
-// warp's float4 loads are 512 contiguous bytes; the block transposes through
-// shared memory and writes the output head-major with each head's dims contiguous.
-constexpr int kReduceDims = 64;
-
+// One CTA per (work row, band of 512 / d_tiles output dims), 256 threads: thread
+// (m, dg) with m = tid & 127 the work row's M row and dg = tid >> 7 the half of each
+// 64-dim chunk it accumulates.  A row's pieces are combined with weights
+// 2^(lse_i - lse) times the value scale (the partials hold O / l in the stored codes'
+// units), lse = log2 of the summed 2^(lse_i).  Slots are laid out [dim / V][row][dim % V]
+// (V = 4 fp32, 8 fp16), so a warp's 16-byte loads are 512 contiguous bytes; the block
+// transposes each 64-dim chunk through shared memory and writes the output row-major.
+// Work rows written whole by the split-KV kernel (one piece) are skipped.
+template <bool F16>
 __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
-  __shared__ float tile[kHeadsPad][kReduceDims + 1];  // [head][dim], padded against bank conflicts
-  const int r = blockIdx.y, d0 = blockIdx.x * kReduceDims;
-  const int h = threadIdx.x & (kHeadsPad - 1), dg = threadIdx.x >> 7;  // 32 dims per thread
-  const WsLayout L = ws_layout(p.B * p.Sq, p.num_clusters);
-  const RowInfo ri = reinterpret_cast<const RowInfo*>(p.ws + L.row_info)[r];
-  float acc[32];
+  grid_dependency_wait();  // the split-KV kernel's partials (programmatic dependent launch)
+  __shared__ float tile[kTileM][64 + 1];  // [row][dim], padded against bank conflicts
+  const int w = blockIdx.y;
+  const WsLayout L = ws_layout(p.B, p.Sq, p.H, p.num_clusters, p.partial_f16);
+  const DealShape d = deal_shape(p.B, p.Sq, p.H, p.num_clusters);
+  const RowInfo ri = reinterpret_cast<const RowInfo*>(p.ws + L.row_info)[w];
+  if (ri.n_parts == 1) return;
+  const int m = threadIdx.x & (kTileM - 1), dg = threadIdx.x >> 7;
+  const int rows_q = p.Sq * p.H;
+  const int b = w / d.Qb, flat0 = kTileM * (w % d.Qb);
+  const bool live = flat0 + m < rows_q;
+  const int np = live ? ri.n_parts : 0;
+  const float* plse = reinterpret_cast<const float*>(p.ws + L.partial_lse) + m;
+  const uint8_t* po = p.ws + L.partial_o;
+  auto slot_of = [&](int i) { return (size_t)ri.first_slot + (size_t)i * d.wb; };
+  // the pieces' LSEs: max, sum, the row's LSE
+  float mx = -INFINITY;
+  for (int i = 0; i < np; ++i) mx = fmaxf(mx, plse[slot_of(i) * kTileM]);
+  const float m0 = mx == -INFINITY ? 0.f : mx;
+  float sum = 0.f;
+  for (int i = 0; i < np; ++i) sum += exp2f(plse[slot_of(i) * kTileM] - m0);
+  const float lse2 = sum > 0.f ? m0 + log2f(sum) : -INFINITY;
+  auto weight = [&](int i) {
+    const float li = plse[slot_of(i) * kTileM];
+    return (sum > 0.f && li != -INFINITY) ? exp2f(li - lse2) * p.ckv_descale : 0.f;
+  };
+  const int band = kDLatent / p.reduce_d_tiles;
+  for (int c = 0; c < band / 64; ++c) {
+    const int d0 = blockIdx.x * band + 64 * c + 32 * dg;  // this thread's 32 dims
+    float acc[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-  float lse2 = -INFINITY;
-  if (h < p.H && ri.n_parts > 0) {
-    const float* plse = reinterpret_cast<const float*>(p.ws + L.partial_lse) + (size_t)ri.first_slot * kHeadsPad + h;
-    const float4* po = reinterpret_cast<const float4*>(p.ws + L.partial_o) +
-                       ((size_t)ri.first_slot * (kDLatent / 4) + (d0 + 32 * dg) / 4) * kHeadsPad + h;
-    const int np = ri.n_parts;
-    // two pieces per round; each round's partial loads are issued before its weights are
-    // known (the first round's before the LSE arithmetic).  An empty piece (LSE -inf, slot
-    // never written) gets weight 0 and is selected away.
-    float4 x[2][8];
-    auto load_round = [&](int i0) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = i0 + u < np ? i0 + u : i0;
-        const float4* src = po + (size_t)i * (kDLatent / 4) * kHeadsPad;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[u][q] = __ldcs(src + (size_t)q * kHeadsPad);
-      }
-    };
-    load_round(0);
-    // the pieces' LSEs: loads issued together, then max and sum
-    float mx = -INFINITY;
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) mx = fmaxf(mx, plse[(size_t)i * kHeadsPad]);
-    const float m0 = mx == -INFINITY ? 0.f : mx;
-    float sum = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) sum += exp2f(plse[(size_t)i * kHeadsPad] - m0);
-    lse2 = sum > 0.f ? m0 + log2f(sum) : -INFINITY;
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+    // two pieces per round, both rounds' loads issued before their weights are applied;
+    // an empty piece (LSE -inf) gets weight 0 and is selected away
     for (int i0 = 0; i0 < np; i0 += 2) {
-      if (i0 > 0) load_round(i0);
-      float w[2];
+      float x[2][32];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const float li = plse[(size_t)(i0 + u < np ? i0 + u : i0) * kHeadsPad];
-        w[u] = (sum > 0.f && i0 + u < np && li != -INFINITY) ? exp2f(li - lse2) : 0.f;
+        const size_t sl = slot_of(i0 + u < np ? i0 + u : i0);
+        if constexpr (F16) {
+          const uint4* src = reinterpret_cast<const uint4*>(po + sl * L.slot_bytes) + m;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldcs(src + (size_t)(d0 / 8 + q) * kTileM);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+              x[u][8 * q + 2 * e] = f.x;
+              x[u][8 * q + 2 * e + 1] = f.y;
+            }
+          }
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(po + sl * L.slot_bytes) + m;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 v = __ldcs(src + (size_t)(d0 / 4 + q) * kTileM);
+            x[u][4 * q] = v.x;
+            x[u][4 * q + 1] = v.y;
+            x[u][4 * q + 2] = v.z;
+            x[u][4 * q + 3] = v.w;
+          }
+        }
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        if (w[u] == 0.f) continue;
+        const float wt = i0 + u < np ? weight(i0 + u) : 0.f;
+        if (wt == 0.f) continue;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          acc[4 * q] += w[u] * x[u][q].x;
-          acc[4 * q + 1] += w[u] * x[u][q].y;
-          acc[4 * q + 2] += w[u] * x[u][q].z;
-          acc[4 * q + 3] += w[u] * x[u][q].w;
+        for (int e = 0; e < 32; ++e) acc[e] += wt * x[u][e];
+      }
+    }
+    // np == 0: no visible key, O = 0
+#pragma unroll
+    for (int e = 0; e < 32; ++e) tile[m][32 * dg + e] = acc[e];
+    __syncthreads();
+    const int hh = threadIdx.x >> 1, part = threadIdx.x & 1;  // one row's 32 dims per thread
+    if (flat0 + hh < rows_q) {
+      const size_t out_row = (size_t)b * rows_q + flat0 + hh;
+      const int od = blockIdx.x * band + 64 * c + 32 * part;
+      const float* t = &tile[hh][32 * part];
+      if (p.out_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row * kDLatent + od);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) dst[v] = make_float4(t[4 * v], t[4 * v + 1], t[4 * v + 2], t[4 * v + 3]);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + out_row * kDLatent + od);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(t[8 * v + 2 * e], t[8 * v + 2 * e + 1]);
+            wv[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          dst[v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
     }
+    __syncthreads();
   }
-  // n_parts == 0: no visible key, O = 0 and LSE = -inf
-#pragma unroll
-  for (int e = 0; e < 32; ++e) tile[h][32 * dg + e] = acc[e];
-  __syncthreads();
-  const int hh = threadIdx.x >> 1, part = threadIdx.x & 1;  // one head's 32 dims per thread
-  if (hh < p.H) {
-    const size_t out_row = (size_t)r * p.H + hh;
-    const float* t = &tile[hh][32 * part];
-    if (p.out_f32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row * kDLatent + d0 + 32 * part);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) dst[v] = make_float4(t[4 * v], t[4 * v + 1], t[4 * v + 2], t[4 * v + 3]);
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + out_row * kDLatent + d0 + 32 * part);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(t[8 * v + 2 * e], t[8 * v + 2 * e + 1]);
-          w[e] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-  }
-  if (p.lse && blockIdx.x == 0 && dg == 0 && h < p.H) p.lse[(size_t)r * p.H + h] = lse2 * 0.69314718055994530942f;
+  if (p.lse && blockIdx.x == 0 && dg == 0 && live)
+    p.lse[(size_t)b * rows_q + flat0 + m] = lse2 * 0.69314718055994530942f;
 }
 
-cudaError_t launch_reduce(const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid(kDLatent / kReduceDims, p.B * p.Sq);
-  reduce_kernel<<<grid, 256, 0, stream>>>(p);
+cudaError_t launch_reduce(const DecodeParams& p, cudaStream_t stream, bool pdl) {
+  const DealShape d = deal_shape(p.B, p.Sq, p.H, p.num_clusters);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.reduce_d_tiles, d.Rw);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return p.partial_f16 ? cudaLaunchKernelEx(&cfg, reduce_kernel<true>, p)
+                       : cudaLaunchKernelEx(&cfg, reduce_kernel<false>, p);
+}
+
+// ------------------------------------------------------------------ context-parallel merge
+// One warp per row, 16 dims per lane: the ranks' pieces of a row (normalized O and
+// natural-log LSE over disjoint key sets) combined with weights e^(lse_r - lse),
+// lse = m + ln(sum_r e^(lse_r - m)); empty pieces (-inf) add nothing, and a row whose
+// pieces are all empty gets O = 0, LSE = -inf.
+template <bool F32>
+__global__ void __launch_bounds__(256) merge_kernel(const void* o_parts, const float* lse_parts, int world,
+                                                    long long rows, void* out, float* lse) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int r = 0; r < world; ++r) mx = fmaxf(mx, lse_parts[(size_t)r * rows + row]);
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  float l = -INFINITY;
+  if (mx != -INFINITY) {
+    float z = 0.f;
+    for (int r = 0; r < world; ++r) z += expf(lse_parts[(size_t)r * rows + row] - mx);
+    l = mx + logf(z);
+    for (int r = 0; r < world; ++r) {
+      const float lr = lse_parts[(size_t)r * rows + row];
+      if (lr == -INFINITY) continue;
+      const float wt = expf(lr - l);
+      const size_t base = ((size_t)r * rows + row) * kDLatent + 16 * lane;
+      if constexpr (F32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(o_parts) + base);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = src[q];
+          acc[4 * q] += wt * v.x;
+          acc[4 * q + 1] += wt * v.y;
+          acc[4 * q + 2] += wt * v.z;
+          acc[4 * q + 3] += wt * v.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o_parts) + base);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint4 v = src[q];
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+            acc[8 * q + 2 * e] += wt * f.x;
+            acc[8 * q + 2 * e + 1] += wt * f.y;
+          }
+        }
+      }
+    }
+  }
+  const size_t obase = (size_t)row * kDLatent + 16 * lane;
+  if constexpr (F32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + obase);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + obase);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t wv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * q + 2 * e], acc[8 * q + 2 * e + 1]);
+        wv[e] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      dst[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+  }
+  if (lse && lane == 0) lse[row] = l;
+}
+
+cudaError_t launch_merge(const void* o_parts, const float* lse_parts, int world, long long rows, int out_f32,
+                         void* out, float* lse, cudaStream_t stream) {
+  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  if (out_f32) merge_kernel<true><<<blocks, 256, 0, stream>>>(o_parts, lse_parts, world, rows, out, lse);
+  else merge_kernel<false><<<blocks, 256, 0, stream>>>(o_parts, lse_parts, world, rows, out, lse);
   return cudaGetLastError();
 }
 
@@ -151,12 +265,13 @@ cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, uint32_t* status_word
 }
 
 // ------------------------------------------------------------------ debug mask
-__global__ void debug_mask_kernel(const int32_t* seq_lens, int Sq, int causal, int window_left, int max_k,
-                                  uint32_t* bits) {
+// One block per (request, token): the decode kernel's visible key range of the row, as bits.
+__global__ void debug_mask_kernel(const DecodeParams p, int max_k, uint32_t* bits) {
   const int row = blockIdx.x;  // b * Sq + t
-  const int b = row / Sq, t = row % Sq;
+  const int b = row / p.Sq, t = row % p.Sq;
+  const int K = clamp_len(p, b, nullptr);
   int lo, hi;
-  visible_range(seq_lens[b], Sq, t, causal, window_left, lo, hi);
+  token_keys(p, b, t, K, global_len(p, b, K), lo, hi);
   const int n_words = (max_k + 31) / 32;
   for (int w = threadIdx.x; w < n_words; w += blockDim.x) {
     uint32_t word = 0;
@@ -168,60 +283,64 @@ __global__ void debug_mask_kernel(const int32_t* seq_lens, int Sq, int causal, i
   }
 }
 
-cudaError_t launch_debug_mask(const int32_t* seq_lens, int B, int Sq, int causal, int window_left, int max_k,
-                              uint32_t* bits, cudaStream_t stream) {
-  debug_mask_kernel<<<B * Sq, 128, 0, stream>>>(seq_lens, Sq, causal, window_left, max_k, bits);
+cudaError_t launch_debug_mask(const DecodeParams& p, int max_k, uint32_t* bits, cudaStream_t stream) {
+  debug_mask_kernel<<<p.B * p.Sq, 128, 0, stream>>>(p, max_k, bits);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ debug gather
-// One CTA per (page of keys, request): the decode kernel's page lookup and TMA
-// boxes bring the page's latent and rope blocks into swizzled shared memory,
-// the slots past the request's length are zeroed as the decode kernel zeroes
-// them, and the block is written back densely.
+// One CTA per (64-key group, request): the decode kernel's page boxes bring the group's
+// latent and rope blocks into swizzled shared memory, the slots past the request's length
+// are zeroed as the decode kernel zeroes them, and the block is written back densely.
 template <bool E4M3>
 __global__ void __launch_bounds__(256) debug_gather_kernel(const __grid_constant__ KvMaps maps,
                                                            const int32_t* page_table, const int32_t* seq_lens,
-                                                           int pt_stride, int num_pages, int max_k, uint8_t* out,
-                                                           uint32_t* err) {
+                                                           int pt_stride, int num_pages, int page_size, int max_k,
+                                                           uint8_t* out, uint32_t* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int es = E4M3 ? 1 : 2;
   constexpr int nlat = latent_blocks<E4M3>();
-  const int lp = blockIdx.x, b = blockIdx.y;
-  const int K = min(max(seq_lens[b], 0), pt_stride * kPageSize);
-  const int key0 = lp * kPageSize;
+  constexpr int rope_row = E4M3 ? 64 : 128;
+  const int grp = blockIdx.x, b = blockIdx.y;
+  const int K = min(max(seq_lens[b], 0), pt_stride * page_size);
+  const int key0 = grp * kKeyGroup;
   if (key0 >= max_k) return;
-  const int valid = min(max(K - key0, 0), kPageSize);
+  const int valid = min(max(K - key0, 0), kKeyGroup);
+  const int nb = boxes_per_group(page_size), br = box_rows(page_size);
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&bar), 1);
     fence_mbar_init();
   }
   __syncthreads();
   if (valid > 0) {
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(smem_addr(&bar), nlat * kBlockBytes + 64 * rope_row);
+    __syncthreads();
+    if (threadIdx.x < nb) {
+      const int i = threadIdx.x;
+      int pg, rw, shift = 0;
       bool bad;
-      const int pg = page_of(page_table, pt_stride, num_pages, b, lp, bad);
+      while ((1 << shift) < page_size) ++shift;
+      box_page(page_table, pt_stride, num_pages, shift, b, key0 + i * br, K, pg, rw, bad);
       if (bad && err) atomicOr(err, kErrBadPage);
-      constexpr uint32_t rope_bytes = E4M3 ? 64 * 64 : kBlockBytes;
-      mbar_arrive_expect_tx(smem_addr(&bar), nlat * kBlockBytes + rope_bytes);
       for (int kb = 0; kb < nlat; ++kb)
-        tma_load_3d(smem_addr(smem + kb * kBlockBytes), &maps.ckv, kb * blk_elems<E4M3>(), 0, pg, smem_addr(&bar));
-      tma_load_3d(smem_addr(smem + nlat * kBlockBytes), &maps.kpe, 0, 0, pg, smem_addr(&bar));
+        tma_load_3d(smem_addr(smem + kb * kBlockBytes + i * br * 128), &maps.ckv, kb * blk_elems<E4M3>(), rw, pg,
+                    smem_addr(&bar));
+      tma_load_3d(smem_addr(smem + nlat * kBlockBytes + i * br * rope_row), &maps.kpe, 0, rw, pg, smem_addr(&bar));
     }
     if (!mbar_wait_bounded(smem_addr(&bar), 0, kWaitTimeoutNs)) {
       if (threadIdx.x == 0 && err) atomicOr(err, kErrTimeout);
       return;
     }
     // slots past the request's length: zero, as the decode kernel does before P.V
-    if (valid < kPageSize)
+    if (valid < kKeyGroup)
       for (int kb = 0; kb < nlat; ++kb) zero_block_rows(smem + kb * kBlockBytes, valid, threadIdx.x, blockDim.x);
     __syncthreads();
   }
-  // write back: row j of this page -> out[b][key0 + j][0:576]
+  // write back: row j of this group -> out[b][key0 + j][0:576]
   const int row_bytes = kDQK * es;
-  const int rows = min(kPageSize, max_k - key0);
+  const int rows = min(kKeyGroup, max_k - key0);
   for (int i = threadIdx.x; i < rows * (row_bytes / 16); i += blockDim.x) {
     const int j = i / (row_bytes / 16), ch = i % (row_bytes / 16);  // 16-byte chunk of the dense row
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -243,21 +362,21 @@ __global__ void __launch_bounds__(256) debug_gather_kernel(const __grid_constant
 }
 
 cudaError_t launch_debug_gather(const KvMaps& maps, bool e4m3, const int32_t* page_table, const int32_t* seq_lens,
-                                int B, int pt_stride, int num_pages, int max_k, void* out, uint32_t* err,
-                                cudaStream_t stream) {
-  dim3 grid((max_k + kPageSize - 1) / kPageSize, B);
+                                int B, int pt_stride, int num_pages, int page_size, int max_k, void* out,
+                                uint32_t* err, cudaStream_t stream) {
+  dim3 grid((max_k + kKeyGroup - 1) / kKeyGroup, B);
   const int smem = 9 * kBlockBytes + 1024;
   cudaError_t e;
   if (e4m3) {
     e = cudaFuncSetAttribute(debug_gather_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    debug_gather_kernel<true><<<grid, 256, smem, stream>>>(maps, page_table, seq_lens, pt_stride, num_pages, max_k,
-                                                            static_cast<uint8_t*>(out), err);
+    debug_gather_kernel<true><<<grid, 256, smem, stream>>>(maps, page_table, seq_lens, pt_stride, num_pages,
+                                                            page_size, max_k, static_cast<uint8_t*>(out), err);
   } else {
     e = cudaFuncSetAttribute(debug_gather_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    debug_gather_kernel<false><<<grid, 256, smem, stream>>>(maps, page_table, seq_lens, pt_stride, num_pages, max_k,
-                                                             static_cast<uint8_t*>(out), err);
+    debug_gather_kernel<false><<<grid, 256, smem, stream>>>(maps, page_table, seq_lens, pt_stride, num_pages,
+                                                             page_size, max_k, static_cast<uint8_t*>(out), err);
   }
   return cudaGetLastError();
 }

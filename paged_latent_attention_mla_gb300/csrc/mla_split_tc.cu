@@ -21,10 +21,16 @@
 // through a small shared buffer, and both halves end with the whole row.  P thus
 // lives in the S stage of its tile: two tiles' P in flight, no shared-memory P
 // buffer held until P.V completes, and no shared-memory reads of A in P.V.
-// The split follows the batch schedule (schedule.cuh); every piece of a row
-// goes to a workspace slot that the reduction kernel turns into the output.  Every mbarrier wait is bounded: on timeout
-// the kernel records kErrTimeout, unwinds its roles, lets in-flight copies
-// land and frees TMEM.
+// A work row is an M tile of 128 (token, head) rows of one request (consecutive
+// tokens pack into it when H < 128); every M row has its own visible key range
+// (its token's causal, window or local bound, on this rank's keys under decode
+// context parallelism).  The split follows the batch schedule (schedule.cuh): a
+// work row cut into several pieces writes each to a workspace slot (fp32, or fp16
+// when asked) that the reduction kernel combines; a work row in one piece is
+// written to the output directly.  Every mbarrier wait is bounded: on timeout the
+// kernel records kErrTimeout, tells its peer CTA, unwinds its roles, and before
+// freeing tensor memory proves with bounded waits that every copy it issued has
+// landed and every MMA it issued has completed.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -40,10 +46,11 @@ namespace tc {
 
 
 constexpr int kThreads = 384;
-constexpr int kMaxSegs = 256;
 // Rescale O only when a row's max grows by more than 2^8: P stays <= 256
 // (exact enough in bf16, below the e4m3 maximum of 448) and most tiles skip it.
 constexpr float kSkipCorrectionLog2 = 8.0f;
+// bounded waits of the abort teardown (anything legitimate lands within microseconds)
+constexpr uint64_t kDrainTimeoutNs = 50000000ull;
 
 template <bool E4M3>
 struct Cfg {
@@ -51,6 +58,7 @@ struct Cfg {
   static constexpr int kNLat = kDLatent / kBlk;  // latent column blocks: 8 or 4
   static constexpr int kNKb = kNLat + 1;         // QK^T contraction blocks (latent + rope)
   static constexpr int kRopeSteps = E4M3 ? 2 : 4;
+  static constexpr int kRopeRow = E4M3 ? 64 : 128;  // bytes of a key's rope row in shared memory
   static constexpr uint32_t kQBytes = kNLat * 8192 + (E4M3 ? 4096 : 8192);
   // P of one row-half of 128 keys in 32-bit words.  The halves swap P through an
   // exchange buffer of [row][half] regions: e4m3 in one round (128 B a region), bf16 in
@@ -60,20 +68,20 @@ struct Cfg {
   static constexpr int kXBytes = 64 * 2 * kXRegion;
   static constexpr int kPCols = E4M3 ? 64 : 128;  // TMEM columns of a full P row
   // One ring of 16 KB slots holds, in consumption order, the K blocks of a tile (one
-  // slot each: this CTA's 128 keys x 128 B) and its V pages (this CTA's columns of 64
-  // keys: two slots in bf16, one per output chunk; one slot in e4m3).
+  // slot each: this CTA's 128 keys x 128 B) and its V key groups (this CTA's columns of
+  // 64 keys: two slots in bf16, one per output chunk; one slot in e4m3).
   static constexpr int kSlot = 16384;
   static constexpr int kNS = E4M3 ? 10 : 8;  // even: each loader warp owns every other slot
   static_assert(kNS % 2 == 0, "the two loader warps own alternate slots");
-  static constexpr int kVItems = E4M3 ? 1 : 2;    // ring slots per V page
-  static constexpr int kPvSteps = E4M3 ? 2 : 4;  // MMAs per page and output chunk (32 or 16 keys each)
+  static constexpr int kVItems = E4M3 ? 1 : 2;    // ring slots per V key group
+  static constexpr int kPvSteps = E4M3 ? 2 : 4;  // MMAs per key group and output chunk (32 or 16 keys each)
   static constexpr uint32_t kIdescQK = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 0);
   static constexpr uint32_t kIdescPV = instr_desc(E4M3 ? 0u : 1u, 128, 256, 0, 1);
   static constexpr int kOffQ = 0;
   static constexpr int kOffX = kOffQ + kNKb * 8192;
   static constexpr int kOffRing = kOffX + kXBytes;
   static constexpr int kOffSeg = kOffRing + kNS * kSlot;
-  static constexpr int kOffMisc = kOffSeg + kMaxSegs * (int)sizeof(Segment);
+  static constexpr int kOffMisc = kOffSeg + kSmemSegs * (int)sizeof(Segment);
 };
 
 struct Misc {
@@ -84,14 +92,24 @@ struct Misc {
   // tile ahead of the correction and of the P.V, never two
   uint64_t pv_ready[2];   // leader: one arrival per CTA, P written and O corrected for the next P.V
   uint64_t pv_local[2];   // this CTA's 4 softmax + 4 correction warps, forwarded to the leader's pv_ready
-  uint64_t tail_ready;    // leader: the peer zeroed the tail of a request's last page (one arrival a slot)
+  uint64_t tail_ready;    // leader: the peer zeroed the tail of a request's last key group (one arrival a slot)
   uint64_t o_done[2];     // P.V of a tile complete
   uint64_t cor_ready[2];  // softmax -> correction: the tile's rescale factor is posted
   uint64_t tail_bar[2], xchg_bar;  // tail_bar: one per loader warp
+  uint64_t drain;                  // abort teardown: the MMA thread's final commit
   float xchg[2][128];             // per-tile row-max exchange between the two halves of a row
   float xsum[128];                // final row-sum exchange
   float corr[2][128];             // per-tile rescale factor, softmax -> correction
   float fin_l[2][128], fin_m[2][128];  // final row statistics, double-buffered by segment
+  // what this CTA issued, for the abort teardown: fills per ring slot, the bytes the
+  // slot's latest fill brings to the leader's barrier (0: a tail fill, which lands on the
+  // loader's own tail barrier), tail fills issued and waited per loader warp, Q loads
+  uint32_t nfill[10], fbytes[10];
+  uint32_t ntail[2], ntail_done[2];
+  // page sizes below 64: each loader warp's page ids of the boxes of three tiles (the one
+  // whose V is loaded, the one whose K is loaded, the next), written by its lanes
+  int32_t boxes[2][3][32];
+  uint32_t nq;
   uint32_t tmem_base;
   uint32_t err;
   uint32_t abort;
@@ -105,25 +123,32 @@ constexpr int smem_bytes() {
 static_assert(smem_bytes<false>() <= 232448, "bf16 kernel exceeds shared memory");
 static_assert(smem_bytes<true>() <= 232448, "e4m3 kernel exceeds shared memory");
 
-// bounded wait that also gives up when another role already aborted
-__device__ __forceinline__ bool kwait(Misc& M, uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// record a timeout and tell both CTAs of the pair to unwind
+__device__ __noinline__ void abort_pair(Misc& M) {
+  atomicOr(&M.err, kErrTimeout);
+  *reinterpret_cast<volatile uint32_t*>(&M.abort) = 1u;
+  st_shared_cluster(map_to_rank(smem_addr(&M.abort), cluster_ctarank() ^ 1u), 1u);
+}
+
+// bounded wait that also gives up when this CTA or its peer already aborted (the spin
+// is out of line: one copy for every wait site keeps the kernel compact)
+__device__ __noinline__ bool kwait_spin(Misc& M, uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*reinterpret_cast<volatile uint32_t*>(&M.abort)) return false;
       if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        atomicOr(&M.err, kErrTimeout);
-        *reinterpret_cast<volatile uint32_t*>(&M.abort) = 1u;
+        abort_pair(M);
         return false;
       }
     }
   }
 }
 
-// the same wait out of line, for call sites whose fast path is inlined
-__device__ __noinline__ bool kwait_slow(Misc& M, uint32_t bar, uint32_t parity) { return kwait(M, bar, parity); }
+__device__ __forceinline__ bool kwait(Misc& M, uint32_t bar, uint32_t parity) {
+  return mbar_try_wait(bar, parity) || kwait_spin(M, bar, parity);
+}
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
@@ -162,7 +187,175 @@ __device__ __forceinline__ int chunk_order(int half, int k) {
   return E4M3 ? (k < 2 ? 1 - k : k) : 3 - k;
 }
 
+// 8 consecutive floats times `scale` to 16 bytes of bf16 or fp16
+__device__ __forceinline__ uint4 pack8_bf16(const uint32_t* r, float scale) {
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(u2f(r[2 * e]) * scale, u2f(r[2 * e + 1]) * scale);
+    w[e] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint4 pack8_f16(const uint32_t* r, float scale) {
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    __half2 h2 = __floats2half2_rn(u2f(r[2 * e]) * scale, u2f(r[2 * e + 1]) * scale);
+    w[e] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+
+// Abort teardown (a bounded wait gave up in this CTA or its peer): before the memory goes
+// away, prove with bounded waits that every copy the pair issued has landed and every MMA
+// has completed.  Of each ring slot only the latest fill can be outstanding (a fill waits
+// for the MMA to consume the one before), and its phase completes on the leader's barrier
+// once the leader armed it and both CTAs' bytes landed: the leader arms a fill only the
+// peer issued, and completes the bytes of a fill only the leader issued.  Tail fills land
+// on each loader's own barrier.  All threads of the CTA call it (it ends in a barrier).
 template <bool E4M3>
+__device__ __noinline__ void drain_after_abort(Misc& M, uint32_t rank, int warp, int lane, int tid) {
+  using C = Cfg<E4M3>;
+  if (rank == 0 && tid == 0) {
+    const uint32_t peer = 1u;
+    for (int sl = 0; sl < C::kNS; ++sl) {
+      const uint32_t a = M.nfill[sl], bcnt = ld_shared_cluster(map_to_rank(smem_addr(&M.nfill[sl]), peer));
+      const uint32_t nf = a > bcnt ? a : bcnt;
+      if (nf == 0) continue;
+      const uint32_t f = nf - 1;
+      const uint32_t bytes = a == nf ? M.fbytes[sl] : ld_shared_cluster(map_to_rank(smem_addr(&M.fbytes[sl]), peer));
+      const uint32_t bar = smem_addr(&M.full[sl]);
+      if (bytes == 0 || mbar_try_wait(bar, f & 1)) continue;
+      if (a < nf) mbar_arrive_expect_tx(bar, bytes);
+      if (bcnt < nf) mbar_complete_tx(bar, bytes);
+      mbar_wait_bounded(bar, f & 1, kDrainTimeoutNs);
+    }
+    const uint32_t a = M.nq, bcnt = ld_shared_cluster(map_to_rank(smem_addr(&M.nq), peer));
+    const uint32_t nq = a > bcnt ? a : bcnt;
+    if (nq > 0) {
+      const uint32_t bar = smem_addr(&M.q_full);
+      if (!mbar_try_wait(bar, (nq - 1) & 1)) {
+        if (a < nq) mbar_arrive_expect_tx(bar, C::kQBytes);
+        if (bcnt < nq) mbar_complete_tx(bar, C::kQBytes);
+        mbar_wait_bounded(bar, (nq - 1) & 1, kDrainTimeoutNs);
+      }
+    }
+  }
+  if (warp >= 10 && lane == 0) {
+    const int own = warp - 10;
+    if (M.ntail[own] > M.ntail_done[own])
+      mbar_wait_bounded(smem_addr(&M.tail_bar[own]), M.ntail_done[own] & 1, kDrainTimeoutNs);
+  }
+  // the MMA thread's final commit arrives on both CTAs' drain barrier once all its MMAs
+  // (and their shared-memory reads) are complete
+  if (warp == 8 && lane == 0 && rank == 0) mma_commit_pair(smem_addr(&M.drain), 0x3);
+  if (warp == 8 && lane == 0) mbar_wait_bounded(smem_addr(&M.drain), 0, kDrainTimeoutNs);
+  __syncthreads();
+}
+
+// The request's last key group, when its length is not a multiple of 64 (loader warp
+// `own`): each CTA landed the group locally on its tail barrier; wait for it, zero the
+// slots' rows past the length (any bits there, NaN included, must not reach P.V), then
+// the leader completes its slots' phases and the peer reports on the leader's
+// tail_ready (the MMA waits for both on this group).  Out of line: once per piece.
+template <bool E4M3>
+__device__ __noinline__ bool tail_group(Misc& M, uint8_t* smem, int own, uint32_t rank, int lane, uint32_t tph,
+                                        int slot0, int slot1, bool mine0, bool mine1, int tail_rows) {
+  using C = Cfg<E4M3>;
+  if (!kwait(M, smem_addr(&M.tail_bar[own]), tph & 1)) return false;
+  if (lane == 0) M.ntail_done[own] += 1;
+#pragma unroll
+  for (int it = 0; it < C::kVItems; ++it) {
+    const bool mine = it == 0 ? mine0 : mine1;
+    const int slot = it == 0 ? slot0 : slot1;
+    if (mine)
+      for (int u = 0; u < 2; ++u) zero_block_rows(smem + C::kOffRing + slot * C::kSlot + u * 8192, tail_rows, lane, 32);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+#pragma unroll
+    for (int it = 0; it < C::kVItems; ++it) {
+      const bool mine = it == 0 ? mine0 : mine1;
+      const int slot = it == 0 ? slot0 : slot1;
+      if (!mine) continue;
+      if (rank == 0)
+        mbar_arrive(smem_addr(&M.full[slot]));
+      else
+        mbar_arrive_cluster(map_to_rank(smem_addr(&M.tail_ready), 0));
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
+// Epilogue of one piece for this thread's M row (correction warps, once per piece): a
+// work row in one piece goes to the output (O / l times the value scale, natural-log
+// LSE); a piece of a longer row goes to its slot (O / l in the stored codes' units and
+// the base-2 LSE, combined and scaled by the reduction kernel).  A row with no visible
+// key in the piece gets O = 0 and LSE = -inf.  TMEM columns [128 c', +128) of this lane
+// hold D columns 256 c' + 128 half + [0, 128).  Out of line: it runs once per piece.
+__device__ __noinline__ void piece_epilogue(const DecodeParams& p, uint8_t* slot_o, float* slot_lse, uint32_t obase,
+                                            int half, int m, int b, int flat, bool live, bool direct, float lrow,
+                                            float mrow) {
+  const bool empty = !(lrow > 0.f);
+  const int rows_q = p.Sq * p.H;
+  if (direct) {
+    // P.V ran on the stored codes of c: the value scale (the key cache's descale) applies here
+    const float inv = empty ? 0.f : p.ckv_descale / lrow;
+    const size_t orow = (size_t)b * rows_q + flat;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(obase + c * 32, r);
+      tmem_ld_wait();
+      const int d0 = 256 * (c >> 2) + 128 * half + 32 * (c & 3);
+      if (!live) continue;
+      if (p.out_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDLatent + d0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv, u2f(r[4 * q + 2]) * inv,
+                               u2f(r[4 * q + 3]) * inv);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * kDLatent + d0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = pack8_bf16(r + 8 * q, inv);
+      }
+    }
+    if (live && half == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : (mrow + log2f(lrow)) * 0.69314718055994530942f;
+  } else {
+    const float inv = empty ? 0.f : 1.f / lrow;
+    uint8_t* so = slot_o;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(obase + c * 32, r);
+      tmem_ld_wait();
+      const int d0 = 256 * (c >> 2) + 128 * half + 32 * (c & 3);
+      if (!live) continue;
+      if (p.partial_f16) {
+        // [dim / 8][row][dim % 8] halves: a warp's 16-byte stores are 512 contiguous bytes
+        uint4* po = reinterpret_cast<uint4*>(so) + m;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) __stcg(po + (size_t)(d0 / 8 + q) * kTileM, pack8_f16(r + 8 * q, inv));
+      } else {
+        float4* po = reinterpret_cast<float4*>(so) + m;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          __stcg(po + (size_t)(d0 / 4 + q) * kTileM, make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv,
+                                                                u2f(r[4 * q + 2]) * inv, u2f(r[4 * q + 3]) * inv));
+      }
+    }
+    if (live && half == 0) slot_lse[m] = empty ? -INFINITY : mrow + log2f(lrow);
+  }
+}
+
+// E4M3: e4m3 inputs (else bf16).  ONE_BOX: page_size >= 64, one page box per 64-key group
+// (else 64 / page_size boxes, looked up through the loader's shared table).
+template <bool E4M3, bool ONE_BOX>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     split_kv_tc(const __grid_constant__ DecodeParams p, const __grid_constant__ KvMaps maps) {
   using C = Cfg<E4M3>;
@@ -176,18 +369,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const int cl = blockIdx.x >> 1;
+  const WsLayout WL = ws_layout(p.B, p.Sq, p.H, p.num_clusters, p.partial_f16);
+  const DealShape DS = deal_shape(p.B, p.Sq, p.H, p.num_clusters);
+  const int rows_q = p.Sq * p.H;  // (token, head) rows of a request
+  Segment* overflow = reinterpret_cast<Segment*>(p.ws + WL.segs) + (size_t)blockIdx.x * WL.seg_cap;
 
   if (tid == 0) {
     M.err = 0;
     M.abort = 0;
+    for (int i = 0; i < 10; ++i) M.nfill[i] = M.fbytes[i] = 0;
+    M.ntail[0] = M.ntail[1] = M.ntail_done[0] = M.ntail_done[1] = 0;
+    M.nq = 0;
   }
   __syncthreads();
   {
     // the batch schedule, in the ring memory before any tile lands there
     int32_t* scratch = reinterpret_cast<int32_t*>(smem + C::kOffRing);
-    ScheduleView sv = build_schedule(p, scratch, &M.err);
-    if (blockIdx.x == 0) write_row_table(p, sv);
-    if (tid == 0) M.nseg = build_segments(p, sv, cl, segs, kMaxSegs, &M.err);
+    Sched sc = build_schedule(p, scratch, &M.err);
+    if (blockIdx.x * blockDim.x < DS.Rw) write_row_table(p, sc);  // the CTAs that own rows of the table
+    if (warp == 0) {
+      const int nseg = build_segments(p, sc, cl, segs, overflow);
+      if (lane == 0) M.nseg = nseg;
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -208,6 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&M.tail_bar[0]), 1);
     mbar_init(smem_addr(&M.tail_bar[1]), 1);
     mbar_init(smem_addr(&M.xchg_bar), 4);
+    mbar_init(smem_addr(&M.drain), 1);
     fence_mbar_init();
   }
   if (warp == 8) {
@@ -227,6 +431,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = M.tmem_base;
   const int nseg = M.nseg;
   auto lead = [&](uint64_t& bar) { return map_to_rank(smem_addr(&bar), 0); };
+  auto seg_at = [&](int s) -> Segment { return s < kSmemSegs ? segs[s] : overflow[s - kSmemSegs]; };
 
   if (warp < 4) {
     // ------------------------------------------------------------ softmax
@@ -237,9 +442,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t xph = 0;
     bool ok = true;
     for (int s = 0; s < nseg && ok; ++s) {
-      const Segment sg = segs[s];
-      int key_lo, key_hi;
-      visible_range(clamp_len(p, sg.row / p.Sq, nullptr), p.Sq, sg.row % p.Sq, p.causal, p.window_left, key_lo, key_hi);
+      const Segment sg = seg_at(s);
+      // this thread's M row: its token's visible keys (none for a padding row)
+      const int b = sg.row() / DS.Qb, flat = kTileM * (sg.row() % DS.Qb) + 64 * (int)rank + row;
+      int key_lo = 0, key_hi = 0;
+      if (flat < rows_q) token_keys(p, b, flat / p.H, sg.K, global_len(p, b, sg.K), key_lo, key_hi);
       const int n = sg.tile_end - sg.tile_begin;
       float m_ref = -INFINITY, l = 0.f;
       for (int i = 0; i < n; ++i, ++j) {
@@ -253,7 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // tiles); the mask is one unsigned compare, so the loops stay branch-free
         const int vlo = full ? 0 : min(max(key_lo - key0, 0), 128);
         const int vhi = full ? 128 : min(max(key_hi - key0, 0), 128);
-        const uint32_t vspan = static_cast<uint32_t>(vhi - vlo);
+        const uint32_t vspan = static_cast<uint32_t>(max(vhi - vlo, 0));
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
@@ -277,8 +484,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_addr(&M.xchg_bar));
         if (!(ok = kwait(M, smem_addr(&M.xchg_bar), xph & 1))) break;
         ++xph;
+        // -inf when no key of this tile is visible to the row (a packed row of an earlier
+        // token, a window edge): its P is then all zero and its statistics stay empty
         const float mt = fmaxf(mloc, M.xchg[j & 1][L ^ 64]);
-        const float mts = mt * cl2;  // finite: every tile holds a visible key of the row
+        const float mts = mt * cl2;
         float m_new, fac;
         if (i == 0) {
           m_new = mts;
@@ -415,12 +624,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int L = tid - 128, row = L & 63, half = L >> 6;
     const uint32_t lanebase = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const uint32_t obase = tmem + lanebase + 256;
-    const WsLayout WL = ws_layout(p.B * p.Sq, p.num_clusters);
-    const int head = 64 * rank + row;
+    const int m = 64 * (int)rank + row;  // this thread's M row
     int j = 0;
     bool ok = true;
     for (int s = 0; s < nseg && ok; ++s) {
-      const Segment sg = segs[s];
+      const Segment sg = seg_at(s);
       const int n = sg.tile_end - sg.tile_begin;
       for (int i = 0; i < n; ++i, ++j) {
         const int st = j & 1;
@@ -452,34 +660,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // epilogue: O / l and the base-2 log-sum-exp to this piece's workspace slot (the
-      // reduction kernel combines a row's pieces, or copies a whole row, into the output).
-      // Slots are [dim / 4][head][dim % 4]: a warp's float4 store, four dims of 32
-      // consecutive heads, is 512 contiguous bytes.
+      // epilogue: the piece to the output or to its slot
       if (!(ok = kwait(M, smem_addr(&M.o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1))) break;
       tc_fence_after();
-      const float lrow = M.fin_l[s & 1][L], mrow = M.fin_m[s & 1][L];
-      // P.V ran on the stored codes of c: the value scale (the key cache's descale) applies here
-      const float inv = p.ckv_descale / lrow;
-      const float lse2 = mrow + log2f(lrow);
-      const bool live = head < p.H;
-      const size_t slot = (size_t)sg.row + cl;
-      float4* po = reinterpret_cast<float4*>(p.ws + WL.partial_o) + slot * (kDLatent / 4) * kHeadsPad + head;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[32];
-        tmem_ld32(obase + c * 32, r);
-        tmem_ld_wait();
-        // TMEM columns [128 chunk, +128) of this lane hold D columns 256 chunk + 128 half + [0, 128)
-        const int d0 = 256 * (c >> 2) + 128 * half + 32 * (c & 3);
-        if (live) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            __stcg(po + (size_t)(d0 / 4 + q) * kHeadsPad, make_float4(u2f(r[4 * q]) * inv, u2f(r[4 * q + 1]) * inv,
-                                                                    u2f(r[4 * q + 2]) * inv, u2f(r[4 * q + 3]) * inv));
-        }
-      }
-      if (live && half == 0) reinterpret_cast<float*>(p.ws + WL.partial_lse)[slot * kHeadsPad + head] = lse2;
+      const int b = sg.row() / DS.Qb, flat = kTileM * (sg.row() % DS.Qb) + m;
+      const int slot = sg.slot();
+      const size_t sl = slot < 0 ? 0 : (size_t)slot;
+      piece_epilogue(p, p.ws + WL.partial_o + sl * WL.slot_bytes,
+                     reinterpret_cast<float*>(p.ws + WL.partial_lse) + sl * kTileM, obase, half, m, b, flat,
+                     flat < rows_q, slot < 0, M.fin_l[s & 1][L], M.fin_m[s & 1][L]);
       tc_fence_before();
     }
   } else if (warp == 8) {
@@ -488,14 +677,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int j = 0, pvc = 0, tcount = 0;
       int rslot = 0;        // next ring slot in consumption order
       uint32_t rphase = 0;  // and the parity of its fill
-      int npages = 0, tail_rows = 0;  // of the current piece's request
+      int ngroups = 0, tail_rows = 0;  // of the current piece's request
       bool ok = true;
       // next ring slot: wait until both CTAs' copies landed (one CTA-scope test in the
       // common case, the bounded wait otherwise)
       auto take = [&](uint32_t& addr, int& slot) -> bool {
         slot = rslot;
         const uint32_t bar = smem_addr(&M.full[rslot]);
-        if (!mbar_try_wait_cta(bar, rphase) && !kwait_slow(M, bar, rphase)) return false;
+        if (!mbar_try_wait_cta(bar, rphase) && !kwait_spin(M, bar, rphase)) return false;
         addr = sRing + slot * C::kSlot;
         if (++rslot == C::kNS) {
           rslot = 0;
@@ -544,13 +733,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int it = 0; it < C::kVItems; ++it)
             if (!take(va[it], slot[it])) return false;
-          if (4 * tile + vp == npages - 1 && tail_rows != 0) {
-            // the request's last page: the peer zeroed its slots' tail too
+          if (4 * tile + vp == ngroups - 1 && tail_rows != 0) {
+            // the request's last key group: the peer zeroed its slots' tail too
             if (!kwait(M, smem_addr(&M.tail_ready), tcount & 1)) return false;
             ++tcount;
           }
           tc_fence_after();
-          // output chunk c's V columns: e4m3 at 8 KB into the page's slot, bf16 in slot c;
+          // output chunk c's V columns: e4m3 at 8 KB into the group's slot, bf16 in slot c;
           // step t moves 16 (bf16) or 32 (e4m3) keys of 128 B down
           const uint64_t vd0 = smem_desc_sw128(va[0], 8192, 1024);
           const uint64_t vd1 = E4M3 ? vd0 + (8192 >> 4) : smem_desc_sw128(va[1], 8192, 1024);
@@ -571,11 +760,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return true;
       };
       for (int s = 0; s < nseg && ok; ++s) {
-        const Segment sg = segs[s];
+        const Segment sg = seg_at(s);
         const int n = sg.tile_end - sg.tile_begin;
-        const int K = clamp_len(p, sg.row / p.Sq, nullptr);
-        npages = (K + kPageSize - 1) / kPageSize;
-        tail_rows = K % kPageSize;
+        ngroups = cdiv(sg.K, kKeyGroup);
+        tail_rows = sg.K % kKeyGroup;
         if (!(ok = kwait(M, smem_addr(&M.q_full), s & 1))) break;
         tc_fence_after();
         for (int i = 0; i < n && ok; ++i) {
@@ -598,20 +786,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t bar = lead(M.q_full);
         // the leader arms the barrier with both CTAs' bytes; the peer's copies only complete bytes on it
         if (rank == 0) mbar_arrive_expect_tx(smem_addr(&M.q_full), 2 * C::kQBytes);
-        const int row = segs[s].row;
+        const int wr = seg_at(s).row(), b = wr / DS.Qb;
+        const int r0 = kTileM * (wr % DS.Qb) + 64 * (int)rank;  // this CTA's 64 (token, head) rows
         for (int kb = 0; kb < C::kNLat; ++kb)
-          tma_load_3d_pair(sQ + kb * 8192, &maps.q_latent, kb * C::kBlk, 64 * rank, row, bar);
-        tma_load_3d_pair(sQ + C::kNLat * 8192, &maps.q_rope, 0, 64 * rank, row, bar);
+          tma_load_3d_pair(sQ + kb * 8192, &maps.q_latent, kb * C::kBlk, r0, b, bar);
+        tma_load_3d_pair(sQ + C::kNLat * 8192, &maps.q_rope, 0, r0, b, bar);
+        M.nq = s + 1;
       }
     }
   } else if (warp >= 10) {
-    // ------------------------------------------------------------ K blocks and V pages, one ring
+    // ------------------------------------------------------------ K blocks and V key groups, one ring
     // Consumption order of each piece: K(t0), then K(t), V(t - 1) for the following tiles,
-    // then V(last); a K block is this CTA's two pages x 128 B of columns, a V page this CTA's
-    // output columns of one page.  Two warps issue the copies: warp 10 the even fills, warp
-    // 11 the odd ones.  The slot count is even, so a slot always has the same owner, and an
-    // owner only ever waits for the release of its own previous fill of the slot.
+    // then V(last); a K block is this CTA's two key groups x 128 B of columns, a V key group
+    // this CTA's output columns of 64 keys.  Two warps issue the copies: warp 10 the even
+    // fills, warp 11 the odd ones.  The slot count is even, so a slot always has the same
+    // owner, and an owner only ever waits for the release of its own previous fill of the
+    // slot.  Lane k of the owning warp issues the tile's box k (page boxes: tma_pages.cuh).
     const int own = warp - 10;
+    const int nb = ONE_BOX ? 1 : boxes_per_group(p.page_size), br = ONE_BOX ? kKeyGroup : box_rows(p.page_size);
+    constexpr bool one_box = ONE_BOX;
+    int32_t* table = &M.boxes[own][0][0];
     int fill = 0;
     uint32_t tph = 0;
     bool ok = true;
@@ -624,142 +818,176 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++fill;
       return true;
     };
+    // Page boxes of a tile, loaded a tile ahead into registers and used a tile later, so
+    // the page-table reads never stall the issuing lane (the validity check is a select and
+    // a bad page id is reported at the end of the piece).  page_size >= 64: one box per key
+    // group, every lane holds the four; below 64: lane k holds box k and writes its page to
+    // the warp's table when the tile comes up, where the issuing lane reads it.  Copies are
+    // issued by lane 0: the loader's per-fill latency is on the ring's critical path.
+    struct TileBoxes {
+      int pg[4], rw[4];
+    };
     for (int s = 0; s < nseg && ok; ++s) {
-      const Segment sg = segs[s];
-      const int b = sg.row / p.Sq;
-      const int K = clamp_len(p, b, nullptr);
-      const int npages = (K + kPageSize - 1) / kPageSize;
-      const int tail_rows = K % kPageSize;
-      auto page_ids = [&](int tile, int (&pg)[4]) {
-        for (int q = 0; q < 4; ++q) {
-          const int lp = 4 * tile + q;
-          bool bad = false;
-          pg[q] = lp < npages ? page_of(p.page_table, p.pt_stride, p.num_pages, b, lp, bad) : p.num_pages;
-          if (bad && lane == 0) atomicOr(&M.err, kErrBadPage);
+      const Segment sg = seg_at(s);
+      const int b = sg.row() / DS.Qb;
+      const int K = sg.K;
+      const int ngroups = cdiv(K, kKeyGroup);
+      const int tail_rows = K % kKeyGroup;
+      bool bad_page = false;
+      auto fetch = [&](int tile, TileBoxes& tb) {
+        bool bad;
+        if constexpr (one_box) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            box_page(p.page_table, p.pt_stride, p.num_pages, p.page_shift, b, tile * kTileN + q * kKeyGroup, K,
+                     tb.pg[q], tb.rw[q], bad);
+            bad_page |= bad;
+          }
+        } else if (lane < 4 * nb) {
+          box_page(p.page_table, p.pt_stride, p.num_pages, p.page_shift, b, tile * kTileN + lane * br, K, tb.pg[0],
+                   tb.rw[0], bad);
+          bad_page |= bad;
+        } else {
+          tb.pg[0] = p.num_pages;
         }
       };
-      auto load_k = [&](int tile, const int (&pg)[4]) -> bool {
+      // below 64: this lane's box of the tile into the warp's table (three tiles in use)
+      auto publish = [&](int tile, const TileBoxes& tb) {
+        if constexpr (one_box) return;
+        table[(tile % 3) * 32 + lane] = tb.pg[0];
+        __syncwarp();
+      };
+      // page and row of box k (k < 4 nb) of a tile, in the issuing lane
+      auto box = [&](const TileBoxes& tb, int tile, int k, int& pg, int& rw) {
+        if constexpr (one_box) {
+          // selects, not a runtime index: the boxes stay in registers
+          pg = k == 0 ? tb.pg[0] : k == 1 ? tb.pg[1] : k == 2 ? tb.pg[2] : tb.pg[3];
+          rw = k == 0 ? tb.rw[0] : k == 1 ? tb.rw[1] : k == 2 ? tb.rw[2] : tb.rw[3];
+        } else {
+          pg = table[(tile % 3) * 32 + k];
+          rw = 0;
+        }
+      };
+      auto load_k = [&](int tile, const TileBoxes& tb) -> bool {
         for (int kb = 0; kb < C::kNKb; ++kb) {
           int slot;
           bool mine;
           if (!acquire(slot, mine)) return false;
           if (mine && lane == 0) {
             const bool rope = kb == C::kNLat;
+            const int rowb = rope ? C::kRopeRow : 128;  // bytes per key row of the block
             const uint32_t bar = lead(M.full[slot]);
             const uint32_t dst = sRing + slot * C::kSlot;
-            const int rb = rope && E4M3 ? 4096 : 8192;
-            if (rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot]), 4 * rb);  // both CTAs' two pages
-            for (int q = 0; q < 2; ++q) {
-              const int page = pg[2 * rank + q];
-              if (!rope) tma_load_3d_pair(dst + q * rb, &maps.ckv, kb * C::kBlk, 0, page, bar);
-              else tma_load_3d_pair(dst + q * rb, &maps.kpe, 0, 0, page, bar);
+            // both CTAs' two key groups
+            if (rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot]), 4 * 64 * rowb);
+            const int k0 = 2 * (int)rank * nb;  // this CTA's boxes: key groups 2 rank, 2 rank + 1
+            for (int q = 0; q < 2 * nb; ++q) {
+              int pg, rw;
+              box(tb, tile, k0 + q, pg, rw);
+              const uint32_t d = dst + q * br * rowb;
+              if (!rope) tma_load_3d_pair(d, &maps.ckv, kb * C::kBlk, rw, pg, bar);
+              else tma_load_3d_pair(d, &maps.kpe, 0, rw, pg, bar);
             }
+            M.nfill[slot] += 1;
+            M.fbytes[slot] = 2 * 64 * rowb;
           }
           __syncwarp();
         }
         return true;
       };
-      auto load_v = [&](int tile, const int (&pg)[4]) -> bool {
+      auto load_v = [&](int tile, const TileBoxes& tb) -> bool {
         for (int vp = 0; vp < 4; ++vp) {
           int slot[2];
           bool mine[2];
           int nmine = 0;
+#pragma unroll
           for (int it = 0; it < C::kVItems; ++it) {
             if (!acquire(slot[it], mine[it])) return false;
             nmine += mine[it] ? 1 : 0;
           }
-          const bool tail = 4 * tile + vp == npages - 1 && tail_rows != 0 && nmine != 0;
+          const bool tail = 4 * tile + vp == ngroups - 1 && tail_rows != 0 && nmine != 0;
           // this CTA's 128-byte column blocks of V: bf16 blocks {0,1,4,5} or {2,3,6,7}
           // (two per slot, one slot per output chunk), e4m3 blocks {rank, 2 + rank}
+          const uint32_t tbar = smem_addr(&M.tail_bar[own]);
           if (lane == 0) {
-            const uint32_t tbar = smem_addr(&M.tail_bar[own]);
             if (tail) mbar_arrive_expect_tx(tbar, nmine * C::kSlot);
+#pragma unroll
             for (int it = 0; it < C::kVItems; ++it) {
               if (!mine[it]) continue;
               const uint32_t dst = sRing + slot[it] * C::kSlot;
               const uint32_t bar = lead(M.full[slot[it]]);
               if (!tail && rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot[it]]), 2 * C::kSlot);
-              for (int u = 0; u < 2; ++u) {
-                const int gb = E4M3 ? 2 * u + (int)rank : 4 * it + 2 * (int)rank + u;
-                if (tail) tma_load_3d(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg[vp], tbar);
-                else tma_load_3d_pair(dst + u * 8192, &maps.ckv, gb * C::kBlk, 0, pg[vp], bar);
+              for (int q = 0; q < nb; ++q) {
+                int pg, rw;
+                box(tb, tile, vp * nb + q, pg, rw);
+                for (int u = 0; u < 2; ++u) {
+                  const int gb = E4M3 ? 2 * u + (int)rank : 4 * it + 2 * (int)rank + u;
+                  const uint32_t d = dst + u * 8192 + q * br * 128;
+                  if (tail) tma_load_3d(d, &maps.ckv, gb * C::kBlk, rw, pg, tbar);
+                  else tma_load_3d_pair(d, &maps.ckv, gb * C::kBlk, rw, pg, bar);
+                }
               }
+              M.nfill[slot[it]] += 1;
+              M.fbytes[slot[it]] = tail ? 0u : (uint32_t)C::kSlot;
             }
+            if (tail) M.ntail[own] += 1;
           }
           __syncwarp();
           if (tail) {
-            // last page of the request: each CTA lands it locally and zeroes the slots past
-            // its length; the leader then completes its slots' phases, the peer reports on
-            // tail_ready (the MMA waits for both on this page)
-            if (!kwait(M, smem_addr(&M.tail_bar[own]), tph & 1)) return false;
+            if (!tail_group<E4M3>(M, smem, own, rank, lane, tph, slot[0], slot[C::kVItems - 1], mine[0],
+                                  mine[C::kVItems - 1], tail_rows))
+              return false;
             ++tph;
-            for (int it = 0; it < C::kVItems; ++it)
-              if (mine[it])
-                for (int u = 0; u < 2; ++u)
-                  zero_block_rows(smem + C::kOffRing + slot[it] * C::kSlot + u * 8192, tail_rows, lane, 32);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              for (int it = 0; it < C::kVItems; ++it) {
-                if (!mine[it]) continue;
-                if (rank == 0)
-                  mbar_arrive(smem_addr(&M.full[slot[it]]));
-                else
-                  mbar_arrive_cluster(lead(M.tail_ready));
-              }
-            }
-            __syncwarp();
           }
         }
         return true;
       };
-      int pg_prev[4], pg_cur[4], pg_next[4];
-      page_ids(sg.tile_begin, pg_cur);
+      TileBoxes prev, cur, next;
+      fetch(sg.tile_begin, cur);
       for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile) {
-        if (tile + 1 < sg.tile_end) page_ids(tile + 1, pg_next);  // read a tile ahead
-        ok = load_k(tile, pg_cur);
-        if (ok && tile > sg.tile_begin) ok = load_v(tile - 1, pg_prev);
-        for (int q = 0; q < 4; ++q) {
-          pg_prev[q] = pg_cur[q];
-          pg_cur[q] = pg_next[q];
-        }
+        if (tile + 1 < sg.tile_end) fetch(tile + 1, next);  // read a tile ahead
+        publish(tile, cur);
+        ok = load_k(tile, cur);
+        if (ok && tile > sg.tile_begin) ok = load_v(tile - 1, prev);
+        prev = cur;
+        cur = next;
       }
-      if (ok) ok = load_v(sg.tile_end - 1, pg_prev);
+      if (ok) ok = load_v(sg.tile_end - 1, prev);
+      if (__any_sync(0xffffffffu, bad_page) && own == 0 && lane == 0) atomicOr(&M.err, kErrBadPage);
     }
   }
 
   // ------------------------------------------------------------ teardown
   __syncwarp();
-  if (*reinterpret_cast<volatile uint32_t*>(&M.abort)) {
-    // let copies and MMAs already in flight finish before the memory goes away
-    for (int i = 0; i < 200; ++i) nanosleep_ns(1000);
-  }
+  grid_launch_dependents();
+  __syncthreads();
+  tc_fence_before();
+  cluster_sync();  // both CTAs have stopped issuing; an abort of either is visible in both
+  tc_fence_after();
+  if (*reinterpret_cast<volatile uint32_t*>(&M.abort)) drain_after_abort<E4M3>(M, rank, warp, lane, tid);
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
   if (warp == 8) tmem_dealloc_pair(tmem, 512);
-  if (tid == 0) {
-    const WsLayout WL = ws_layout(p.B * p.Sq, p.num_clusters);
-    reinterpret_cast<uint32_t*>(p.ws + WL.cta_status)[2 * cl + rank] = M.err;
-  }
+  if (tid == 0) reinterpret_cast<uint32_t*>(p.ws + WL.cta_status)[2 * cl + rank] = M.err;
 }
 
 }  // namespace tc
 
-cudaError_t launch_split_kv(const DecodeParams& p, const KvMaps& maps, cudaStream_t stream) {
+template <bool E4M3, bool ONE_BOX>
+static cudaError_t launch_variant(const DecodeParams& p, const KvMaps& maps, cudaStream_t stream) {
   const dim3 grid(2 * p.num_clusters), block(tc::kThreads);
-  if (p.qkv_e4m3) {
-    const int smem = tc::smem_bytes<true>();
-    cudaError_t e = cudaFuncSetAttribute(tc::split_kv_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    tc::split_kv_tc<true><<<grid, block, smem, stream>>>(p, maps);
-  } else {
-    const int smem = tc::smem_bytes<false>();
-    cudaError_t e = cudaFuncSetAttribute(tc::split_kv_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    tc::split_kv_tc<false><<<grid, block, smem, stream>>>(p, maps);
-  }
+  const int smem = tc::smem_bytes<E4M3>();
+  cudaError_t e = cudaFuncSetAttribute(tc::split_kv_tc<E4M3, ONE_BOX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tc::split_kv_tc<E4M3, ONE_BOX><<<grid, block, smem, stream>>>(p, maps);
   return cudaGetLastError();
+}
+
+cudaError_t launch_split_kv(const DecodeParams& p, const KvMaps& maps, cudaStream_t stream) {
+  const bool one = p.page_size >= kKeyGroup;
+  if (p.qkv_e4m3) return one ? launch_variant<true, true>(p, maps, stream) : launch_variant<true, false>(p, maps, stream);
+  return one ? launch_variant<false, true>(p, maps, stream) : launch_variant<false, false>(p, maps, stream);
 }
 
 int split_kv_max_clusters(int device, bool e4m3) {
@@ -779,12 +1007,12 @@ int split_kv_max_clusters(int device, bool e4m3) {
   cudaError_t e;
   if (e4m3) {
     cfg.dynamicSmemBytes = tc::smem_bytes<true>();
-    cudaFuncSetAttribute(tc::split_kv_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
-    e = cudaOccupancyMaxActiveClusters(&n, tc::split_kv_tc<true>, &cfg);
+    cudaFuncSetAttribute(tc::split_kv_tc<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+    e = cudaOccupancyMaxActiveClusters(&n, tc::split_kv_tc<true, true>, &cfg);
   } else {
     cfg.dynamicSmemBytes = tc::smem_bytes<false>();
-    cudaFuncSetAttribute(tc::split_kv_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
-    e = cudaOccupancyMaxActiveClusters(&n, tc::split_kv_tc<false>, &cfg);
+    cudaFuncSetAttribute(tc::split_kv_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+    e = cudaOccupancyMaxActiveClusters(&n, tc::split_kv_tc<false, true>, &cfg);
   }
   if (e != cudaSuccess || n <= 0) return sms / 2;
   return n;

@@ -274,3 +274,28 @@ __host__ __device__ constexpr uint64_t smem_desc_sw64(uint32_t addr, uint32_t sb
 
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 }  // namespace mla
+
+namespace mla {
+// Complete `bytes` of the pending transaction count of a barrier in this CTA without a
+// copy: accounts for bytes a copy that was never issued would have brought.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// 32-bit load / store of a shared variable of another CTA of the cluster (shared::cluster address)
+__device__ __forceinline__ uint32_t ld_shared_cluster(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel of the stream start its launch
+// (it waits for this grid's completion before reading what this grid wrote), and wait
+// for the previous kernel's completion before reading what it wrote.  Both are no-ops
+// for a launch without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+}  // namespace mla

@@ -49,55 +49,93 @@ def cfg(**kw):
     return n.make_config(**base)
 
 
-def host_plan(lens, Sq, causal, window, G, tile=256, piece_cost=1):
-    """Independent restatement of the batch deal: each row with visible keys costs piece_cost virtual
-    tiles followed by its real tiles; the rows' virtual tiles end to end are dealt in equal contiguous
-    shares to min(G, T) clusters; a row's pieces are the clusters whose share meets its real tiles."""
-    rows = []
-    for K in lens:
-        for t in range(Sq):
-            hi = K - (Sq - 1 - t) if causal else K
-            lo = K - Sq - window + t if window >= 0 else 0
-            hi, lo = min(max(hi, 0), K), min(max(lo, 0), K)
-            lo = min(lo, hi)
-            rows.append(0 if hi <= lo else (hi + tile - 1) // tile - lo // tile)
-    cost = [nt + piece_cost if nt else 0 for nt in rows]
-    T = sum(cost)
-    Ge = max(1, min(G, T))
-    shares = [(c * T // Ge, (c + 1) * T // Ge) for c in range(Ge)]
-    assert all(e > b for b, e in shares) or T == 0
-    parts, start = [], 0
-    for nt, ct in zip(rows, cost):
-        lo, hi = start + piece_cost, start + piece_cost + nt
-        parts.append(sum(1 for b, e in shares if b < hi and lo < e) if nt else 0)
-        start += ct
-    return len(rows), max([1] + parts)
+def host_plan(lens, Sq, H, causal, window, G, tile=256, piece_cost=1):
+    """Independent restatement of the batch deal.
+
+    A request's Sq*H (token, head) rows, token-major, form work rows of 128.  A group of
+    wb = min(work rows per request, G) clusters takes a request's work rows side by side;
+    each sub-band (wb consecutive work rows of a request) costs piece_cost virtual tiles
+    plus the tiles of the union of its rows' visible keys.  The sub-bands' virtual tiles
+    end to end are dealt in equal contiguous shares to min(G // wb, T) groups; a work row's
+    pieces are the groups whose share meets its own tiles.  Returns (slots, most pieces)."""
+    def keys(K, t):
+        hi = K - (Sq - 1 - t) if causal else K
+        lo = K - Sq - window + t if window >= 0 else 0
+        hi, lo = min(max(hi, 0), K), min(max(lo, 0), K)
+        return min(lo, hi), hi
+
+    def span(K, tokens):
+        rng = [keys(K, t) for t in tokens]
+        rng = [(lo, hi) for lo, hi in rng if hi > lo]
+        if not rng:
+            return 0, 0
+        lo, hi = min(r[0] for r in rng), max(r[1] for r in rng)
+        return lo // tile, -(-hi // tile) - lo // tile
+
+    rows_q = Sq * H
+    Qb = -(-rows_q // 128)
+    wb = min(Qb, G)
+    nsub = -(-Qb // wb)
+    Gg = max(1, G // wb)
+
+    def tokens_of(i0, i1):
+        return range(128 * i0 // H, (min(rows_q, 128 * (i1 + 1)) - 1) // H + 1)
+
+    subs = []  # (b, k, ulo, U)
+    for b, K in enumerate(lens):
+        for k in range(nsub):
+            ulo, U = span(K, tokens_of(k * wb, min(Qb, k * wb + wb) - 1))
+            subs.append((b, k, ulo, U))
+    starts, T = [], 0
+    for _, _, _, U in subs:
+        starts.append(T)
+        T += U + piece_cost if U else 0
+    Gd = max(1, min(Gg, T))
+    shares = [(g * T // Gd, (g + 1) * T // Gd) for g in range(Gd)]
+    most = 1
+    for s, (b, k, ulo, U) in enumerate(subs):
+        for i in range(k * wb, min(Qb, k * wb + wb)):
+            tlo, n = span(lens[b], tokens_of(i, i))
+            if not n:
+                continue
+            x0 = starts[s] + piece_cost + (tlo - ulo)
+            most = max(most, sum(1 for g0, g1 in shares if g0 < x0 + n and x0 < g1))
+    return (len(subs) + Gg) * wb, most
 
 
-@pytest.mark.parametrize("lens,Sq,causal,window,G", [
-    ([4096] * 64, 1, False, -1, 76),
-    ([100, 257], 1, False, -1, 76),
-    ([16384] * 32, 2, True, -1, 76),
-    ([131072] * 8, 4, True, 4096, 76),
-    ([1, 2, 3, 5000, 0, 77], 3, True, 100, 5),
-    ([300] * 7, 1, False, -1, 1),
+@pytest.mark.parametrize("lens,Sq,H,causal,window,G", [
+    ([4096] * 64, 1, 128, False, -1, 76),
+    ([100, 257], 1, 16, False, -1, 76),
+    ([16384] * 32, 2, 128, True, -1, 76),
+    ([131072] * 8, 4, 128, True, 4096, 76),
+    ([1, 2, 3, 5000, 0, 77], 3, 128, True, 100, 5),
+    ([300] * 7, 1, 128, False, -1, 1),
+    ([900, 40, 3000], 8, 16, True, -1, 76),
+    ([700, 5, 1500], 5, 48, True, 200, 76),
+    ([2000, 64], 64, 16, True, -1, 3),
 ])
-def test_plan_matches_independent_schedule(lib, lens, Sq, causal, window, G):
+def test_plan_matches_independent_schedule(lib, lens, Sq, H, causal, window, G):
     stride = max(1, (max(lens) + 63) // 64)
     c = cfg(seq_len_q=Sq, causal=causal, page_table_stride=stride, num_clusters=G)
-    split, ws = n.mla_plan(lens, len(lens), 128, 64, window, c)
-    R, want_split = host_plan(lens, Sq, causal, window, G)
+    split, ws = n.mla_plan(lens, len(lens), H, 64, window, c)
+    slots, want_split = host_plan(lens, Sq, H, causal, window, G)
     assert split == want_split
-    slots = R + G
     # the workspace holds at least the fp32 partials and their LSEs for every slot
     assert ws >= slots * 128 * (512 + 1) * 4
     assert ws % 256 == 0
+    c16 = cfg(seq_len_q=Sq, causal=causal, page_table_stride=stride, num_clusters=G, partial_fp16=True)
+    _, ws16 = n.mla_plan(lens, len(lens), H, 64, window, c16)
+    assert slots * 128 * (256 + 1) * 4 <= ws16 < ws
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(H=0), n.MLA_ERR_INVALID_ARG),
     (dict(H=129), n.MLA_ERR_UNSUPPORTED),
-    (dict(page_size=32), n.MLA_ERR_UNSUPPORTED),
+    (dict(page_size=48), n.MLA_ERR_UNSUPPORTED),  # not a power of two
+    (dict(page_size=4), n.MLA_ERR_UNSUPPORTED),  # below one 8-row swizzle group
+    (dict(page_size=2048), n.MLA_ERR_UNSUPPORTED),
+    (dict(cfg=dict(cp_world=2, cp_rank=2)), n.MLA_ERR_INVALID_ARG),
+    (dict(cfg=dict(reducer_d_tiles=3)), n.MLA_ERR_INVALID_ARG),
     (dict(window_left=-2), n.MLA_ERR_INVALID_ARG),
     (dict(cfg=dict(q_descale=0.5)), n.MLA_ERR_INVALID_ARG),  # bf16 inputs take no scales
     (dict(cfg=dict(qkv_dtype=torch.float8_e4m3fn, ckv_descale=0.5, kpe_descale=0.25)), n.MLA_ERR_UNSUPPORTED),
@@ -156,4 +194,6 @@ def test_decode_rejects_before_launch(lib):
     assert decode_status(ws=FakeTensor(0x100080, nbytes=1 << 30)) == n.MLA_ERR_INVALID_ARG  # workspace not 256-aligned
     assert decode_status(ws=FakeTensor(0x100000, nbytes=1024)) == n.MLA_ERR_WORKSPACE_TOO_SMALL
     assert decode_status(cfg=dict(seq_len_q=0)) == n.MLA_ERR_INVALID_ARG
-    assert decode_status(ckv=FakeTensor(0x30000, (64, 32, 512))) == n.MLA_ERR_UNSUPPORTED  # page size 32
+    assert decode_status(ckv=FakeTensor(0x30000, (64, 48, 512))) == n.MLA_ERR_UNSUPPORTED  # page size 48
+    # context parallelism needs the whole sequences' lengths
+    assert decode_status(cfg=dict(cp_world=2, cp_rank=1)) == n.MLA_ERR_INVALID_ARG
