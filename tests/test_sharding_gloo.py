@@ -83,80 +83,59 @@ def test_two_rank_shards_equal_whole_batch():
     assert slow == 2.0
 
 
-# Decode context parallelism, exercised on CPU ranks: every request's pages are dealt to
-# the ranks in turn (logical page j to rank j % world), each rank decodes its own keys, the
-# ranks exchange (O, LSE) and the pieces merge with the split-KV combine, in natural log:
-# lse = m + ln(sum_r e^(lse_r - m)) and O = sum_r e^(lse_r - lse) O_r.  With Sq = 1 and no
-# causal mask a row's softmax does not depend on the order of its keys, so a rank's piece
-# is the decode of its keys as a request of their own.
+# Decode context parallelism, exercised on CPU ranks: each rank holds its share of every
+# request's keys (workloads.dcp_shard: runs of cp_interleave positions dealt in turn),
+# decodes its share under the whole sequence's bounds, and the product's exchange
+# (sharding.dcp_exchange, an all-gather) brings the ranks' (O, LSE) shares together in the
+# layout mla_merge takes.  The shares come from the oracle here (no GPU) and are combined
+# with the oracle's merge; the GPU tests run the CUDA decode and the CUDA merge.
 
-def _dcp_local(p, world, rank):
-    from paged_latent_attention_mla_gb300.workloads import PAD_PAGE
-
-    pt, sl = p["page_table"], p["seq_lens"]
-    P = p["ckv"].shape[1]
-    B = pt.shape[0]
-    width = max(1, (pt.shape[1] + world - 1) // world)
-    lpt = torch.full((B, width), PAD_PAGE, dtype=torch.int32)
-    lsl = torch.zeros(B, dtype=torch.int32)
-    for b in range(B):
-        K = int(sl[b])
-        mine = [j for j in range((K + P - 1) // P) if j % world == rank]
-        for i, j in enumerate(mine):
-            lpt[b, i] = pt[b, j]
-        lsl[b] = sum(min(P, K - j * P) for j in mine)  # a partial page is the request's last
-    return dict(p, page_table=lpt, seq_lens=lsl)
-
-
-def _merge(O_parts, L_parts):
-    L = np.stack(L_parts)  # [world, rows]
-    m = np.max(L, axis=0)
-    m0 = np.where(np.isfinite(m), m, 0.0)
-    s = np.sum(np.exp(L - m0), axis=0)
-    lse = np.where(s > 0, m0 + np.log(np.where(s > 0, s, 1.0)), -np.inf)
-    w = np.where(np.isfinite(L), np.exp(L - np.where(np.isfinite(lse), lse, 0.0)), 0.0)
-    return np.einsum("rn,rnd->nd", w, np.stack(O_parts)), lse
-
-
-def _dcp_worker(rank, world, port, q):
+def _dcp_worker(rank, world, interleave, port, q):
     import torch.distributed as dist
 
     import oracle
     from paged_latent_attention_mla_gb300 import workloads as wl
+    from paged_latent_attention_mla_gb300.sharding import dcp_exchange
 
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        # lengths with a request on one page only, so some ranks hold no key of it
-        prob = wl.make_problem("tiny", H=3, seq_lens=[100, 257, 64, 1, 300, 129], B=6)
-        p = prob.host_inputs()
-        O, L = oracle.decode(_dcp_local(p, world, rank), threads=1)
-        mine = torch.from_numpy(np.concatenate([O.reshape(-1), L.reshape(-1)]))
-        outs = [torch.zeros_like(mine) for _ in range(world)]
-        dist.all_gather(outs, mine)
+        # causal query blocks with a window, and requests too short for some ranks to hold a key
+        prob = wl.make_problem("tiny", H=3, Sq=3, causal=True, window_left=70, seq_lens=[100, 257, 64, 1, 300, 129],
+                               B=6)
+        sh = wl.dcp_shard(prob, world, rank, interleave)
+        O, L = oracle.decode_ex(sh.host_inputs(), cp_world=world, cp_rank=rank, cp_interleave=interleave,
+                                global_seq_lens=sh.extra["global_seq_lens"], threads=1)
+        B, Sq, H = prob.B, prob.Sq, prob.H
+        out = torch.from_numpy(O).reshape(B, Sq, H, 512)
+        lse = torch.from_numpy(L).reshape(B, Sq, H)
+        o_parts, lse_parts = dcp_exchange(out, lse)
+        ok = tuple(o_parts.shape) == (world, B, Sq, H, 512) and tuple(lse_parts.shape) == (world, B, Sq, H)
+        ok = ok and torch.equal(o_parts[rank], out) and torch.equal(lse_parts[rank], lse)
         if rank == 0:
-            n = O.shape[0]
-            parts = [o.numpy() for o in outs]
-            Om, Lm = _merge([v[: n * 512].reshape(n, 512) for v in parts], [v[n * 512:] for v in parts])
-            Of, Lf = oracle.decode(p, threads=1)
+            n = B * Sq * H
+            Om, Lm = oracle.merge([o.reshape(n, 512).numpy() for o in o_parts.unbind(0)],
+                                  [x.reshape(n).numpy() for x in lse_parts.unbind(0)])
+            Of, Lf = oracle.decode(prob.host_inputs(), threads=1)
             fin = np.isfinite(Lf)
-            ok = (np.array_equal(np.isfinite(Lm), fin) and np.all(Om[~fin] == 0)
-                  and np.abs(Lm[fin] - Lf[fin]).max() <= 1e-12
-                  and np.abs(Om - Of).max() <= 1e-12 * max(np.abs(Of).max(), 1e-300))
-            q.put(bool(ok))
+            ok = ok and (np.array_equal(np.isfinite(Lm), fin) and np.all(Om[~fin] == 0)
+                         and np.abs(Lm[fin] - Lf[fin]).max() <= 1e-12
+                         and np.abs(Om - Of).max() <= 1e-12 * max(np.abs(Of).max(), 1e-300))
+        q.put((rank, bool(ok)))
     finally:
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3])
-def test_dcp_merge_over_cpu_ranks_equals_whole_decode(world):
+@pytest.mark.parametrize("world,interleave", [(2, 1), (3, 4)])
+def test_dcp_exchange_over_cpu_ranks_merges_to_whole_decode(world, interleave):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_dcp_worker, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_dcp_worker, args=(r, world, interleave, port, q)) for r in range(world)]
     for pr in procs:
         pr.start()
     for pr in procs:
         pr.join(timeout=240)
     assert all(pr.exitcode == 0 for pr in procs)
-    assert q.get(timeout=5)
+    results = dict(q.get(timeout=5) for _ in range(world))
+    assert all(results[r] for r in range(world))
