@@ -226,6 +226,15 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def decode_options(args, prob) -> dict:
+    """Decoder options the run asks for: the wrapper's defaults (PDL reduction, fp16 partials
+    for e4m3) unless told otherwise."""
+    opts = {"use_pdl": not args.no_pdl}
+    if args.partial_fp16:
+        opts["partial_fp16"] = True
+    return opts
+
+
 def ev_pair():
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -235,7 +244,7 @@ def measure(name, args, world, rank, local_rank, peaks, peak_src):
     alone, the call through host buffers, and the call without the flush."""
     prob = wl.make_problem(name, seed=rank_seed(wl.WORKLOADS[name].seed, rank))
     d = prob.device_inputs("cuda")
-    dec = decoder_for(prob)
+    dec = decoder_for(prob, **decode_options(args, prob))
     flops, kv = algorithmic_counts(prob)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -419,6 +428,8 @@ def main():
                     help="all (default): the uniform headline plus records for varlen, fp8spec and window")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
+    ap.add_argument("--partial-fp16", action="store_true", help="fp16 split partials for bf16 caches too")
+    ap.add_argument("--no-pdl", action="store_true", help="launch the reduction without programmatic dependent launch")
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per reference-arm step")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

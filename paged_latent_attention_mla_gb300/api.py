@@ -29,8 +29,11 @@ class PagedMlaDecoder:
     def __init__(self, *, H: int, seq_len_q: int, num_pages: int, page_table_stride: int, qkv_dtype,
                  out_dtype=torch.bfloat16, causal: bool = False, window_left: int = -1, q_descale: float = 1.0,
                  kv_descale: float = 1.0, num_clusters: int = 0, page_size: int = PAGE_SIZE, cp_world: int = 1,
-                 cp_rank: int = 0, cp_interleave: int = 1, partial_fp16: bool = False, reducer_d_tiles: int = 0,
-                 use_pdl: bool = False, device="cuda"):
+                 cp_rank: int = 0, cp_interleave: int = 1, partial_fp16=None, reducer_d_tiles: int = 0,
+                 use_pdl: bool = True, device="cuda"):
+        # fp16 partials by default where the stored value codes always fit fp16 (e4m3, |x| <= 448)
+        if partial_fp16 is None:
+            partial_fp16 = qkv_dtype == torch.float8_e4m3fn
         self.H, self.Sq = H, seq_len_q
         self.window_left = window_left
         self.out_dtype = out_dtype

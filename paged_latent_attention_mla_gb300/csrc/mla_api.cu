@@ -92,6 +92,7 @@ int plan_max_parts(const int32_t* seq_lens, int B, int H, int page_size, int win
                    int G) {
   const int Sq = cfg->seq_len_q;
   const DealShape d = deal_shape(B, Sq, H, G);
+  const int pu = piece_units(cfg->qkv_dtype == MLA_E4M3);
   const bool exact = cp_world_of(cfg) == 1 && !cfg->local_visible_lens;
   auto span = [&](int b, int t0, int t1, int& tlo, int& n) {
     int K = seq_lens[b];
@@ -115,7 +116,7 @@ int plan_max_parts(const int32_t* seq_lens, int B, int H, int page_size, int win
     int t0, t1;
     work_tokens(k * d.wb, std::min(d.Qb, k * d.wb + d.wb) - 1, Sq, H, t0, t1);
     span(b, t0, t1, ulo[s], U[s]);
-    prefix[s + 1] = prefix[s] + (U[s] > 0 ? U[s] + kPieceCost : 0);
+    prefix[s + 1] = prefix[s] + (U[s] > 0 ? pu + kUnitsPerTile * U[s] : 0);
   }
   const long long T = prefix[d.S];
   const int Gd = deal_groups(d.Gg, T);
@@ -126,8 +127,8 @@ int plan_max_parts(const int32_t* seq_lens, int B, int H, int page_size, int win
     work_tokens(i, i, Sq, H, t0, t1);
     span(b, t0, t1, tlo, n);
     if (n <= 0) continue;
-    const long long xf = prefix[s] + kPieceCost + (tlo - ulo[s]);
-    most = std::max(most, group_of_tile(xf + n - 1, T, Gd) - group_of_tile(xf, T, Gd) + 1);
+    const long long xf = tile_unit(prefix[s], pu, tlo - ulo[s]), xl = tile_unit(prefix[s], pu, tlo - ulo[s] + n - 1);
+    most = std::max(most, group_of_tile(xl, T, Gd) - group_of_tile(xf, T, Gd) + 1);
   }
   return most;
 }
@@ -212,6 +213,7 @@ DecodeParams make_params(const void* q_latent, const void* q_rope, const void* c
   p.qkv_e4m3 = cfg->qkv_dtype == MLA_E4M3 ? 1 : 0;
   p.out_f32 = cfg->out_dtype == MLA_F32 ? 1 : 0;
   p.partial_f16 = cfg->partial_fp16 ? 1 : 0;
+  p.piece_units = piece_units(p.qkv_e4m3 != 0);
   p.num_clusters = G;
   p.reduce_d_tiles = d_tiles_of(cfg);
   p.scale = scale;

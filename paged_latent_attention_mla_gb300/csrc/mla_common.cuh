@@ -21,10 +21,14 @@ constexpr int kMaxHeads = kTileM;
 constexpr int kMinPageSize = 8;     // one 8-row group of the 128-byte swizzle
 constexpr int kMaxPageSize = 1024;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded device waits give up after 2 s
-// The batch deal charges every (sub-)band with visible keys this many virtual tiles ahead of
-// its real ones: what starting a piece costs a cluster (its Q, the pipeline refill, the
-// epilogue), so that a cluster dealt many short rows gets fewer tiles.
-constexpr int kPieceCost = 1;
+// The batch deal counts work in units of a quarter tile: a tile of 256 keys is 4 units,
+// and every (sub-)band with visible keys is charged piece_units ahead of its tiles, what
+// starting a piece costs a cluster (its Q, the pipeline refill, the epilogue), so that a
+// cluster dealt many short rows gets fewer tiles.  Measured on GB300 (3 to 6 units swept
+// over the benchmark batches), a whole tile is best: below it batches of many short rows
+// overload the clusters dealt them, above it nothing gains.
+constexpr int kUnitsPerTile = 4;
+__host__ __device__ constexpr int piece_units(bool) { return kUnitsPerTile; }
 // Segments (pieces of work) each CTA keeps in shared memory; a cluster dealt more keeps
 // the rest in its workspace region.
 constexpr int kSmemSegs = 256;
@@ -50,6 +54,7 @@ struct DecodeParams {
   int B, Sq, H, num_pages, pt_stride, page_size, page_shift, causal, window_left;
   int cp_world, cp_rank, cp_interleave;
   int qkv_e4m3, out_f32, partial_f16;
+  int piece_units;             // the deal's charge for starting a piece (quarter tiles)
   int num_clusters;            // clusters launched (G)
   int reduce_d_tiles;          // CTAs per work row across the 512 output dims (1, 2, 4 or 8)
   float scale;                 // softmax scale
@@ -114,9 +119,13 @@ __host__ __device__ inline void tile_span(int lo, int hi, int& tile_lo, int& n_t
 // with G clusters launched, a group of wb = min(Qb, G) clusters walks the same tiles of a
 // request together, lane j of the group taking work rows j, j + wb, ... (sub-band k holds
 // work rows [k wb, k wb + wb)).  Super-row s = b * nsub + k is one sub-band; it costs
-// kPieceCost + U virtual tiles, U the tiles of the union of its work rows' spans.  The
-// super-rows' virtual tiles are laid end to end (prefix sums) and dealt in equal contiguous
-// shares to Gd = min(G / wb, T) groups: group g owns virtual tiles [g T / Gd, (g+1) T / Gd).
+// piece_units + 4 U units, U the tiles of the union of its work rows' spans.  The
+// super-rows' units are laid end to end (prefix sums) and dealt in equal contiguous shares
+// to Gd = min(G / wb, T / 4) groups (every share at least one tile's worth): group g owns
+// units [g T / Gd, (g+1) T / Gd), and a tile belongs to the group whose share holds its
+// first unit.  Tile i of super-row s (counted from the sub-band's first tile) starts at
+// unit prefix[s] + piece_units + 4 i; inside a row's tiles any 4 consecutive units hold
+// one tile start, so every group between a row's first and last piece owns tiles of it.
 //
 // Slots.  The piece of work row k wb + j that group g computes writes partial slot
 // (s + g) * wb + j: the groups holding one super-row are consecutive, so these never
@@ -152,8 +161,8 @@ __host__ __device__ inline void work_tokens(int i0, int i1, int Sq, int H, int& 
   t1 = last / H;
 }
 
-// group holding virtual tile x when T virtual tiles are dealt to Gd groups in equal
-// contiguous shares [floor(g*T/Gd), floor((g+1)*T/Gd))
+// group holding unit x when T units are dealt to Gd groups in equal contiguous shares
+// [floor(g*T/Gd), floor((g+1)*T/Gd))
 // (32-bit arithmetic when the products fit, as they do for any batch of practical size)
 __host__ __device__ inline int group_of_tile(long long x, long long T, long long Gd) {
   if (T < (1 << 20) && Gd <= 2048) return (int)((((uint32_t)x + 1u) * (uint32_t)Gd - 1u) / (uint32_t)T);
@@ -165,9 +174,16 @@ __host__ __device__ inline long long group_tile_begin(long long g, long long T, 
   return g * T / Gd;
 }
 
-// groups the T virtual tiles are dealt to: never more than T, so none is empty
+// groups the T units are dealt to: every share at least one tile's worth of units
 __host__ __device__ inline int deal_groups(int Gg, long long T) {
-  return T < 1 ? 1 : (T < Gg ? (int)T : Gg);
+  const long long most = T / kUnitsPerTile;
+  return most < 1 ? 1 : (most < Gg ? (int)most : Gg);
+}
+
+// first unit of tile i (counted from the sub-band's first tile) of a super-row whose
+// units start at `start`
+__host__ __device__ inline long long tile_unit(long long start, int pu, int i) {
+  return start + pu + (long long)kUnitsPerTile * i;
 }
 
 // -------------------------------------------------------------- workspace

@@ -120,7 +120,7 @@ __device__ __forceinline__ Sched build_schedule(const DecodeParams& p, int32_t* 
     const int K = clamp_len(p, b, s % d.nsub == 0 ? err_flag : nullptr);  // a bad length flagged once
     int ulo, U;
     sub_span(p, d, b, s % d.nsub, K, global_len(p, b, K), ulo, U);
-    const int cost = U > 0 ? U + kPieceCost : 0;
+    const int cost = U > 0 ? p.piece_units + kUnitsPerTile * U : 0;
     prefix[s] = cost;
     local += cost;
   }
@@ -161,7 +161,7 @@ __device__ __forceinline__ Sched build_schedule(const DecodeParams& p, int32_t* 
   return sc;
 }
 
-// largest super-row s with prefix[s] <= x (x < T): the super-row holding virtual tile x
+// largest super-row s with prefix[s] <= x (x < T): the super-row holding unit x
 __device__ __forceinline__ int super_row_of_tile(const Sched& sc, long long x) {
   int lo = 0, hi = sc.d.S - 1;
   while (lo < hi) {
@@ -173,14 +173,13 @@ __device__ __forceinline__ int super_row_of_tile(const Sched& sc, long long x) {
 }
 
 // pieces of a work row whose own tiles start tlo - ulo into super-row s: n_parts and the
-// group of its first piece
-__device__ __forceinline__ int row_parts(const Sched& sc, int s, int ulo, int tlo, int n, int& g_first) {
+// group of its first piece (the groups owning its first and last tiles, and every one between)
+__device__ __forceinline__ int row_parts(const Sched& sc, int pu, int s, int ulo, int tlo, int n, int& g_first) {
   if (n <= 0) {
     g_first = 0;
     return 0;
   }
-  const long long pb = (long long)sc.prefix[s] + kPieceCost;
-  const long long xf = pb + (tlo - ulo), xl = xf + n - 1;
+  const long long xf = tile_unit(sc.prefix[s], pu, tlo - ulo), xl = tile_unit(sc.prefix[s], pu, tlo - ulo + n - 1);
   g_first = group_of_tile(xf, sc.T, sc.Gd);
   return group_of_tile(xl, sc.T, sc.Gd) - g_first + 1;
 }
@@ -210,12 +209,16 @@ __device__ __forceinline__ int build_segments(const DecodeParams& p, const Sched
         int ulo, U, tlo, nt;
         sub_span(p, d, b, k, K, Kg, ulo, U);
         work_span(p, b, i, K, Kg, tlo, nt);
-        const long long pb = (long long)sc.prefix[s] + kPieceCost, pe = pb + U;
-        const long long gb = pb > cb ? pb : cb, ge = pe < ce ? pe : ce;
-        const int t_begin = max(ulo + (int)(gb - pb), tlo), t_end = min(ulo + (int)(ge - pb), tlo + nt);
-        if (U > 0 && gb < ge && t_begin < t_end) {
+        // the sub-band's tiles whose first unit lies in [cb, ce): i in [ceil((cb - pb) / 4),
+        // ceil((ce - pb) / 4)), pb the unit of its tile 0; then those of this work row
+        const long long pb = tile_unit(sc.prefix[s], p.piece_units, 0);
+        const long long ib = cb <= pb ? 0 : (cb - pb + kUnitsPerTile - 1) / kUnitsPerTile;
+        const long long ie = ce <= pb ? 0 : (ce - pb + kUnitsPerTile - 1) / kUnitsPerTile;
+        const int t_begin = max(ulo + (int)min(ib, (long long)U), tlo);
+        const int t_end = min(ulo + (int)min(ie, (long long)U), tlo + nt);
+        if (U > 0 && t_begin < t_end) {
           int g_first;
-          const int np = row_parts(sc, s, ulo, tlo, nt, g_first);
+          const int np = row_parts(sc, p.piece_units, s, ulo, tlo, nt, g_first);
           const int slot = np == 1 ? -1 : (s + g) * d.wb + j;
           sg.row_slot = (uint32_t)(b * d.Qb + i) | ((uint32_t)(slot + 1) << 14);
           sg.tile_begin = t_begin;
@@ -256,7 +259,7 @@ __device__ __forceinline__ void write_row_table(const DecodeParams& p, const Sch
     if (n > 0) {
       int ulo, U, g_first;
       sub_span(p, d, b, k, K, Kg, ulo, U);
-      ri.n_parts = row_parts(sc, s, ulo, tlo, n, g_first);
+      ri.n_parts = row_parts(sc, p.piece_units, s, ulo, tlo, n, g_first);
       ri.first_slot = (s + g_first) * d.wb + j;
     }
     info[w] = ri;

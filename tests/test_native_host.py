@@ -49,15 +49,19 @@ def cfg(**kw):
     return n.make_config(**base)
 
 
-def host_plan(lens, Sq, H, causal, window, G, tile=256, piece_cost=1):
+def host_plan(lens, Sq, H, causal, window, G, e4m3=False, tile=256):
     """Independent restatement of the batch deal.
 
     A request's Sq*H (token, head) rows, token-major, form work rows of 128.  A group of
-    wb = min(work rows per request, G) clusters takes a request's work rows side by side;
-    each sub-band (wb consecutive work rows of a request) costs piece_cost virtual tiles
-    plus the tiles of the union of its rows' visible keys.  The sub-bands' virtual tiles
-    end to end are dealt in equal contiguous shares to min(G // wb, T) groups; a work row's
-    pieces are the groups whose share meets its own tiles.  Returns (slots, most pieces)."""
+    wb = min(work rows per request, G) clusters takes a request's work rows side by side.
+    Work is counted in quarter tiles: each sub-band (wb consecutive work rows of a request)
+    costs a piece charge (4 units) plus 4 units per tile of the union of its
+    rows' visible keys.  The sub-bands' units end to end are dealt in equal contiguous
+    shares to min(G // wb, T // 4) groups; a tile goes to the group whose share holds its
+    first unit, and a work row's pieces are the groups owning its tiles.
+    Returns (slots, most pieces)."""
+    piece = 4
+
     def keys(K, t):
         hi = K - (Sq - 1 - t) if causal else K
         lo = K - Sq - window + t if window >= 0 else 0
@@ -89,17 +93,22 @@ def host_plan(lens, Sq, H, causal, window, G, tile=256, piece_cost=1):
     starts, T = [], 0
     for _, _, _, U in subs:
         starts.append(T)
-        T += U + piece_cost if U else 0
-    Gd = max(1, min(Gg, T))
-    shares = [(g * T // Gd, (g + 1) * T // Gd) for g in range(Gd)]
+        T += piece + 4 * U if U else 0
+    Gd = max(1, min(Gg, T // 4))
+    bounds = [g * T // Gd for g in range(Gd + 1)]
+
+    def owner(x):  # group whose share [bounds[g], bounds[g+1]) holds unit x
+        return max(g for g in range(Gd) if bounds[g] <= x)
+
     most = 1
     for s, (b, k, ulo, U) in enumerate(subs):
         for i in range(k * wb, min(Qb, k * wb + wb)):
             tlo, n = span(lens[b], tokens_of(i, i))
             if not n:
                 continue
-            x0 = starts[s] + piece_cost + (tlo - ulo)
-            most = max(most, sum(1 for g0, g1 in shares if g0 < x0 + n and x0 < g1))
+            groups = {owner(starts[s] + piece + 4 * (tlo - ulo + t)) for t in range(n)}
+            assert groups == set(range(min(groups), max(groups) + 1))  # consecutive groups
+            most = max(most, len(groups))
     return (len(subs) + Gg) * wb, most
 
 
@@ -119,6 +128,11 @@ def test_plan_matches_independent_schedule(lib, lens, Sq, H, causal, window, G):
     c = cfg(seq_len_q=Sq, causal=causal, page_table_stride=stride, num_clusters=G)
     split, ws = n.mla_plan(lens, len(lens), H, 64, window, c)
     slots, want_split = host_plan(lens, Sq, H, causal, window, G)
+    assert split == want_split
+    c8 = cfg(seq_len_q=Sq, causal=causal, page_table_stride=stride, num_clusters=G, qkv_dtype=torch.float8_e4m3fn,
+             q_descale=0.5, ckv_descale=0.25, kpe_descale=0.25)
+    split8, _ = n.mla_plan(lens, len(lens), H, 64, window, c8)
+    assert split8 == host_plan(lens, Sq, H, causal, window, G, e4m3=True)[1]
     assert split == want_split
     # the workspace holds at least the fp32 partials and their LSEs for every slot
     assert ws >= slots * 128 * (512 + 1) * 4
