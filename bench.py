@@ -44,12 +44,15 @@ HEADLINE = "uniform"  # the headline value; the other 128-head workloads get rec
 ALL = ["uniform", "varlen", "fp8spec", "window"]
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one split-KV kernel launch,
-# from an ncu capture of the same command (profiles/split_kv_tc_uniform.md, split_kv_tc_fp8spec.md), valid only for
+# from an ncu capture of the same batch (profiles/split_kv_tc_<workload>.md; captured with
+# --compact-pool, the same pages and tiles in a pool small enough to capture), valid only for
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "96ece8eb2eb630649a03b07bb010fd64c0cf0457aa1d9bd6da07b9512113d238", "bytes": 321266688 + 14566400},
-    "fp8spec": {"sources_sha256": "96ece8eb2eb630649a03b07bb010fd64c0cf0457aa1d9bd6da07b9512113d238", "bytes": 568142592 + 17271808},
+    "uniform": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 321493504 + 14273792},
+    "varlen": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 554160896 + 19035904},
+    "fp8spec": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 310223360 + 8945664},
+    "window": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 44956672 + 1562368},
 }
 
 
@@ -242,7 +245,10 @@ def ev_pair():
 def measure(name, args, world, rank, local_rank, peaks, peak_src):
     """One workload: the device-resident call (L2 flushed before each), the split-KV kernel
     alone, the call through host buffers, and the call without the flush."""
-    prob = wl.make_problem(name, seed=rank_seed(wl.WORKLOADS[name].seed, rank))
+    # --compact-pool: only the pages the batch uses (profiling: the same tiles and traffic in a
+    # pool small enough to capture); the default keeps the workload's own pool
+    prob = wl.make_problem(name, seed=rank_seed(wl.WORKLOADS[name].seed, rank),
+                           pool_pages=0 if args.compact_pool else None)
     d = prob.device_inputs("cuda")
     dec = decoder_for(prob, **decode_options(args, prob))
     flops, kv = algorithmic_counts(prob)
@@ -430,6 +436,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
     ap.add_argument("--partial-fp16", action="store_true", help="fp16 split partials for bf16 caches too")
     ap.add_argument("--no-pdl", action="store_true", help="launch the reduction without programmatic dependent launch")
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="allocate only the pages the batch uses (for profiling captures; same tiles and traffic)")
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per reference-arm step")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
