@@ -232,7 +232,7 @@ def run_reference(args, world, rank):
 def decode_options(args, prob) -> dict:
     """Decoder options the run asks for: the wrapper's defaults (PDL reduction, fp16 partials
     for e4m3) unless told otherwise."""
-    opts = {"use_pdl": not args.no_pdl}
+    opts = {"use_pdl": not args.no_pdl, "combine_in_kernel": args.combine_in_kernel}
     if args.partial_fp16:
         opts["partial_fp16"] = True
     return opts
@@ -436,6 +436,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
     ap.add_argument("--partial-fp16", action="store_true", help="fp16 split partials for bf16 caches too")
     ap.add_argument("--no-pdl", action="store_true", help="launch the reduction without programmatic dependent launch")
+    ap.add_argument("--combine-in-kernel", action="store_true",
+                    help="combine split rows inside the split-KV kernel instead of in the reduction kernel")
     ap.add_argument("--compact-pool", action="store_true",
                     help="allocate only the pages the batch uses (for profiling captures; same tiles and traffic)")
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per reference-arm step")

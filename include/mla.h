@@ -108,6 +108,10 @@ typedef enum { MLA_BF16 = 0, MLA_E4M3 = 1, MLA_F32 = 2 } mla_dtype_t;
  *                     1, 2, 4 or 8 (0: 8)
  *  use_pdl            1: launch the reduction with programmatic dependent launch, so its
  *                     launch overlaps the split-KV kernel's end (not with split_timing)
+ *  combine_in_kernel  0 (default): a separate reduction kernel combines the pieces of a row
+ *                     cut into several (reducer_d_tiles, use_pdl); 1: the split-KV kernel
+ *                     combines them, the last piece of a row to finish counting its arrival
+ *                     in the workspace, and mla_decode launches one kernel
  */
 typedef struct {
   int seq_len_q;
@@ -129,6 +133,7 @@ typedef struct {
   int partial_fp16;
   int reducer_d_tiles;
   int use_pdl;
+  int combine_in_kernel;
 } mla_config_t;
 
 /*
@@ -175,8 +180,9 @@ MLA_API mla_status_t mla_plan(const int32_t *seq_lens, int B, int H, int page_si
  *  window_left -1, or the sliding-window span (same value as given to mla_plan)
  *  out        [B, seq_len_q, H, 512] out_dtype
  *  lse        [B, seq_len_q, H] fp32 natural-log LSE, or NULL to skip it
- *  workspace  device scratch of at least the planned size, 256-byte aligned; its
- *             contents need no initialization and are overwritten
+ *  workspace  device scratch of at least the planned size, 256-byte aligned.  Zero it
+ *             once after allocating it (its rows' arrival counters must start at zero or
+ *             hold an earlier call's tag); after that it needs no clearing between calls
  *  stream     the CUDA stream all work is enqueued on
  *
  * Cache slots past a request's length and pages no visible key uses may hold

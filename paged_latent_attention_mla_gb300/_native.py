@@ -51,6 +51,7 @@ class MlaConfig(ctypes.Structure):
         ("partial_fp16", ctypes.c_int),
         ("reducer_d_tiles", ctypes.c_int),
         ("use_pdl", ctypes.c_int),
+        ("combine_in_kernel", ctypes.c_int),
     ]
 
 
@@ -113,7 +114,8 @@ def _stream(stream):
 def make_config(*, seq_len_q: int, num_pages: int, page_table_stride: int, qkv_dtype, out_dtype=torch.bfloat16,
                 causal: bool = False, q_descale: float = 1.0, ckv_descale: float = 1.0, kpe_descale: float = 1.0,
                 num_clusters: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1,
-                partial_fp16: bool = False, reducer_d_tiles: int = 0, use_pdl: bool = False) -> MlaConfig:
+                partial_fp16: bool = False, reducer_d_tiles: int = 0, use_pdl: bool = False,
+                combine_in_kernel: bool = False) -> MlaConfig:
     """The C config; the device pointers global_seq_lens / local_visible_lens are set per call
     (set_call_inputs), since their tensors belong to the call."""
     qd = _DTYPES[qkv_dtype] if isinstance(qkv_dtype, torch.dtype) else int(qkv_dtype)
@@ -122,6 +124,7 @@ def make_config(*, seq_len_q: int, num_pages: int, page_table_stride: int, qkv_d
                   float(q_descale), float(ckv_descale), float(kpe_descale), int(num_clusters))
     c.cp_world, c.cp_rank, c.cp_interleave = int(cp_world), int(cp_rank), int(cp_interleave)
     c.partial_fp16, c.reducer_d_tiles, c.use_pdl = int(bool(partial_fp16)), int(reducer_d_tiles), int(bool(use_pdl))
+    c.combine_in_kernel = int(bool(combine_in_kernel))
     return c
 
 

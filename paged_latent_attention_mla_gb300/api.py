@@ -24,13 +24,15 @@ class PagedMlaDecoder:
     Context parallelism: give cp_world / cp_rank / cp_interleave here and each call's
     global_seq_lens; combine the ranks' outputs with merge_ranks (sharding.py holds the
     exchange).  local_visible_lens, when given to a call, bounds each query token's keys.
+    Rows cut into several pieces are combined by the reduction kernel; combine_in_kernel=True
+    has the split-KV kernel combine them instead (the last piece of a row to finish does it).
     """
 
     def __init__(self, *, H: int, seq_len_q: int, num_pages: int, page_table_stride: int, qkv_dtype,
                  out_dtype=torch.bfloat16, causal: bool = False, window_left: int = -1, q_descale: float = 1.0,
                  kv_descale: float = 1.0, num_clusters: int = 0, page_size: int = PAGE_SIZE, cp_world: int = 1,
                  cp_rank: int = 0, cp_interleave: int = 1, partial_fp16=None, reducer_d_tiles: int = 0,
-                 use_pdl: bool = True, device="cuda"):
+                 use_pdl: bool = True, combine_in_kernel: bool = False, device="cuda"):
         # fp16 partials by default where the stored value codes always fit fp16 (e4m3, |x| <= 448)
         if partial_fp16 is None:
             partial_fp16 = qkv_dtype == torch.float8_e4m3fn
@@ -43,7 +45,8 @@ class PagedMlaDecoder:
                                        qkv_dtype=qkv_dtype, out_dtype=out_dtype, causal=causal, q_descale=q_descale,
                                        ckv_descale=kv_descale, kpe_descale=kv_descale, num_clusters=num_clusters,
                                        cp_world=cp_world, cp_rank=cp_rank, cp_interleave=cp_interleave,
-                                       partial_fp16=partial_fp16, reducer_d_tiles=reducer_d_tiles, use_pdl=use_pdl)
+                                       partial_fp16=partial_fp16, reducer_d_tiles=reducer_d_tiles, use_pdl=use_pdl,
+                                       combine_in_kernel=combine_in_kernel)
         self.workspace = None
         self.split_kv = None
 
@@ -51,7 +54,8 @@ class PagedMlaDecoder:
         sl = torch.as_tensor(seq_lens_host, dtype=torch.int32).cpu()
         self.split_kv, ws_bytes = _native.mla_plan(sl, sl.numel(), self.H, self.page_size, self.window_left, self.cfg)
         if self.workspace is None or self.workspace.numel() < ws_bytes:
-            self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
+            # zeroed once: the rows' arrival counters start at zero (later calls need no clearing)
+            self.workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=self.device)
         return self.split_kv, ws_bytes
 
     def __call__(self, q_latent, q_rope, ckv, kpe, page_table, seq_lens, scale: float, out=None, lse=None,
@@ -72,8 +76,9 @@ class PagedMlaDecoder:
         return out, lse
 
     def launches_per_call(self) -> int:
-        """Kernels one decode call launches: the split-KV kernel and the reduction."""
-        return 2
+        """Kernels one decode call launches: the split-KV kernel, and the reduction kernel
+        unless the split-KV kernel combines the rows itself (combine_in_kernel)."""
+        return 1 if self.cfg.combine_in_kernel else 2
 
     def status(self, stream=None) -> int:
         return _native.mla_workspace_status(self.workspace, stream)

@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -27,7 +28,6 @@ namespace {
 constexpr int kMaxRows = 16384;   // B * seq_len_q (schedule scratch in shared memory)
 constexpr int kMaxSeqLenQ = 64;
 constexpr int kMaxWorld = 1024;
-constexpr int kMaxClusters = 1024;  // the partial slot of a segment has 18 bits
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -49,6 +49,7 @@ mla_status_t validate_cfg(const mla_config_t* cfg, int B, int H, int page_size, 
   if (!pow2(page_size) || page_size < kMinPageSize || page_size > kMaxPageSize) return MLA_ERR_UNSUPPORTED;
   if (H > kMaxHeads || cfg->seq_len_q > kMaxSeqLenQ) return MLA_ERR_UNSUPPORTED;
   if ((long long)B * cfg->seq_len_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * ((cfg->seq_len_q * H + kTileM - 1) / kTileM) > kMaxWorkRows) return MLA_ERR_UNSUPPORTED;
   if (cfg->num_clusters > kMaxClusters) return MLA_ERR_UNSUPPORTED;
   if ((long long)cfg->page_table_stride * page_size > (1ll << 30)) return MLA_ERR_UNSUPPORTED;
   if (cfg->cp_world < 0 || cfg->cp_interleave < 0) return MLA_ERR_INVALID_ARG;
@@ -56,6 +57,7 @@ mla_status_t validate_cfg(const mla_config_t* cfg, int B, int H, int page_size, 
     if (cfg->cp_world > kMaxWorld || cfg->cp_rank < 0 || cfg->cp_rank >= cfg->cp_world) return MLA_ERR_INVALID_ARG;
   }
   if (cfg->partial_fp16 != 0 && cfg->partial_fp16 != 1) return MLA_ERR_INVALID_ARG;
+  if (cfg->combine_in_kernel != 0 && cfg->combine_in_kernel != 1) return MLA_ERR_INVALID_ARG;
   if (cfg->reducer_d_tiles != 0 && cfg->reducer_d_tiles != 1 && cfg->reducer_d_tiles != 2 &&
       cfg->reducer_d_tiles != 4 && cfg->reducer_d_tiles != 8)
     return MLA_ERR_INVALID_ARG;
@@ -181,6 +183,14 @@ bool encode_kv_maps(KvMaps* maps, const void* ckv, const void* kpe, const void* 
   return ok;
 }
 
+// A tag for this call's arrival counters (never 0, so a zeroed workspace matches no call).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> epoch{0};
+  uint32_t e = ++epoch;
+  if (e == 0) e = ++epoch;
+  return e;
+}
+
 // decode parameters from the call's arguments (validated)
 DecodeParams make_params(const void* q_latent, const void* q_rope, const void* ckv_cache, const void* kpe_cache,
                          const int32_t* page_table, const int32_t* seq_lens, float scale, int window_left, void* out,
@@ -214,6 +224,8 @@ DecodeParams make_params(const void* q_latent, const void* q_rope, const void* c
   p.out_f32 = cfg->out_dtype == MLA_F32 ? 1 : 0;
   p.partial_f16 = cfg->partial_fp16 ? 1 : 0;
   p.piece_units = piece_units(p.qkv_e4m3 != 0);
+  p.fused_combine = cfg->combine_in_kernel;
+  p.epoch = next_epoch();
   p.num_clusters = G;
   p.reduce_d_tiles = d_tiles_of(cfg);
   p.scale = scale;
@@ -290,6 +302,7 @@ mla_status_t mla_decode(const void* q_latent, const void* q_rope, const void* ck
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (timed && cudaEventRecord(static_cast<cudaEvent_t>(cfg->split_timing[1]), stream) != cudaSuccess)
     return MLA_ERR_CUDA;
+  if (p.fused_combine) return MLA_OK;  // the split-KV kernel combined every row itself
   // the PDL reduction starts its launch while the split-KV kernel drains; it is not used
   // when the split kernel is timed alone (its end event would then come late)
   return cuda_status(launch_reduce(p, stream, cfg->use_pdl != 0 && !timed));

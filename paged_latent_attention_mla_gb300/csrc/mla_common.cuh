@@ -31,7 +31,7 @@ constexpr int kUnitsPerTile = 4;
 __host__ __device__ constexpr int piece_units(bool) { return kUnitsPerTile; }
 // Segments (pieces of work) each CTA keeps in shared memory; a cluster dealt more keeps
 // the rest in its workspace region.
-constexpr int kSmemSegs = 256;
+constexpr int kSmemSegs = 192;
 
 // status bits each CTA of the split-KV kernel leaves in its own status word
 constexpr uint32_t kErrTimeout = 1u;
@@ -55,6 +55,8 @@ struct DecodeParams {
   int cp_world, cp_rank, cp_interleave;
   int qkv_e4m3, out_f32, partial_f16;
   int piece_units;             // the deal's charge for starting a piece (quarter tiles)
+  int fused_combine;           // the last piece of a row combines it (no reduction kernel)
+  uint32_t epoch;              // this call's tag in the rows' arrival counters
   int num_clusters;            // clusters launched (G)
   int reduce_d_tiles;          // CTAs per work row across the 512 output dims (1, 2, 4 or 8)
   float scale;                 // softmax scale
@@ -219,15 +221,19 @@ struct Segment {
   int32_t tile_begin;  // tiles [tile_begin, tile_end) of the work row
   int32_t tile_end;
   int32_t K;
+  uint32_t parts;      // the row's pieces | this piece's index among them << 16
   __host__ __device__ int row() const { return (int)(row_slot & 0x3FFFu); }
   __host__ __device__ int slot() const { return (int)(row_slot >> 14) - 1; }
+  __host__ __device__ int n_parts() const { return (int)(parts & 0xFFFFu); }
+  __host__ __device__ int piece() const { return (int)(parts >> 16); }
 };
 constexpr int kMaxWorkRows = 1 << 14;
+constexpr int kMaxClusters = 1024;  // the partial slot of a segment has 18 bits
 
 __host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t cta_status, row_info, segs, partial_lse, partial_o, total;
+  size_t cta_status, row_info, counters, segs, partial_lse, partial_o, total;
   size_t slot_bytes;  // bytes of one slot's O
   int seg_cap;        // overflow segments per CTA
 };
@@ -239,7 +245,12 @@ __host__ __device__ inline WsLayout ws_layout(int B, int Sq, int H, int G, int p
   l.slot_bytes = (size_t)kTileM * kDLatent * (partial_f16 ? 2 : 4);
   size_t off = align256(sizeof(WsHeader));
   l.cta_status = off;
-  off = align256(off + sizeof(uint32_t) * 2 * (size_t)G);
+  off = align256(off + sizeof(uint32_t) * 2 * (size_t)kMaxClusters);
+  // [work row][CTA of the pair] arrival counters, epoch << 32 | pieces arrived: at the same
+  // offset and size for every shape, so no other region of an earlier call's layout lands
+  // on them (a zeroed workspace stays valid across plans of any shape)
+  l.counters = off;
+  off = align256(off + sizeof(unsigned long long) * 2 * (size_t)kMaxWorkRows);
   l.row_info = off;
   off = align256(off + sizeof(RowInfo) * (size_t)d.Rw);
   l.segs = off;

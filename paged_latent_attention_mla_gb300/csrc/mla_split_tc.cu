@@ -32,6 +32,7 @@
 // freeing tensor memory proves with bounded waits that every copy it issued has
 // landed and every MMA it issued has completed.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -51,6 +52,9 @@ constexpr int kThreads = 384;
 constexpr float kSkipCorrectionLog2 = 8.0f;
 // bounded waits of the abort teardown (anything legitimate lands within microseconds)
 constexpr uint64_t kDrainTimeoutNs = 50000000ull;
+// work rows a CTA combines at its end: a cluster's share cuts at most the work rows at its
+// two ends, so two (more are combined at once by the correction warps)
+constexpr int kCombList = 4;
 
 template <bool E4M3>
 struct Cfg {
@@ -97,6 +101,7 @@ struct Misc {
   uint64_t cor_ready[2];  // softmax -> correction: the tile's rescale factor is posted
   uint64_t tail_bar[2], xchg_bar;  // tail_bar: one per loader warp
   uint64_t drain;                  // abort teardown: the MMA thread's final commit
+  uint64_t comb_in, comb_out;      // fused combine: the 4 correction warps' partials written; the verdict posted
   float xchg[2][128];             // per-tile row-max exchange between the two halves of a row
   float xsum[128];                // final row-sum exchange
   float corr[2][128];             // per-tile rescale factor, softmax -> correction
@@ -110,6 +115,11 @@ struct Misc {
   // whose V is loaded, the one whose K is loaded, the next), written by its lanes
   int32_t boxes[2][3][32];
   uint32_t nq;
+  // in-kernel combine: the verdict of this CTA's latest arrival (1: combine the row now),
+  // and the work rows it arrived last on, combined at the end (row, first slot, pieces)
+  uint32_t last_piece;
+  uint32_t ncl;
+  int4 comb_list[kCombList];
   uint32_t tmem_base;
   uint32_t err;
   uint32_t abort;
@@ -291,6 +301,148 @@ __device__ __noinline__ bool tail_group(Misc& M, uint8_t* smem, int own, uint32_
   return true;
 }
 
+// In-kernel combine, arrival (the correction warps, 128 threads, once the piece's
+// partial is written): count this CTA's piece of the work row; the last of the row's
+// pieces to arrive combines them.  The counter holds this call's epoch in its high half,
+// so a word left by an earlier call counts as zero.  The last arrival queues the row for
+// the end of the kernel (every role idle then, so more threads and loads in flight), or
+// asks for the combine now when the queue is full.  The two syncs among the correction
+// warps are mbarriers waited with the bounded waits (phase parity `ph`).  Returns 1 to
+// combine now, 0 otherwise, -1 when a wait gave up.
+__device__ __noinline__ int arrive_piece(Misc& M, const DecodeParams& p, unsigned long long* counter, uint32_t ph,
+                                         int w, int first_slot, int np, int L) {
+  __threadfence();  // this thread's partial stores before the arrival
+  __syncwarp();
+  if ((L & 31) == 0) mbar_arrive(smem_addr(&M.comb_in));
+  if (!kwait(M, smem_addr(&M.comb_in), ph)) return -1;
+  if (L == 0) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(counter), seen, want;
+    do {
+      seen = cur;
+      want = (seen >> 32) == p.epoch ? seen + 1 : ((unsigned long long)p.epoch << 32) | 1ull;
+      cur = atomicCAS(counter, seen, want);
+    } while (cur != seen);
+    uint32_t now = 0;
+    if ((uint32_t)(want & 0xFFFFFFFFull) == (uint32_t)np) {
+      const uint32_t k = M.ncl++;
+      if (k < (uint32_t)kCombList) M.comb_list[k] = make_int4(w, first_slot, np, 0);
+      else now = 1;
+    }
+    *reinterpret_cast<volatile uint32_t*>(&M.last_piece) = now;
+    mbar_arrive(smem_addr(&M.comb_out));
+  }
+  if (!kwait(M, smem_addr(&M.comb_out), ph)) return -1;
+  return (int)*reinterpret_cast<volatile uint32_t*>(&M.last_piece);
+}
+
+// In-kernel combine of work row w for this CTA's 64 M rows, as the reduction kernel does:
+// lse = log2 of the summed 2^(lse_i), out = output_scale * sum_i 2^(lse_i - lse) O_i over
+// its np slots (first_slot, wb apart); an empty piece (lse_i = -inf) adds nothing.  nthr
+// threads (a multiple of 64), t this one: M row 64 rank + (t & 63), 32-column blocks
+// t / 64 + k nthr / 64; two pieces' loads are issued before either is applied.
+__device__ __noinline__ void combine_row(const DecodeParams& p, const uint8_t* part_o, const float* part_lse,
+                                         size_t slot_bytes, int w, int first_slot, int np, int wb, int Qb,
+                                         uint32_t rank, int t, int nthr) {
+  __threadfence();  // the other pieces' stores, published before their arrivals
+  const int rows_q = p.Sq * p.H;
+  const int m = 64 * (int)rank + (t & 63);
+  const int flat = kTileM * (w % Qb) + m;
+  if (flat >= rows_q) return;
+  const float* plse = part_lse + m;
+  float mx = -INFINITY;
+  for (int i = 0; i < np; ++i) mx = fmaxf(mx, __ldcg(plse + (size_t)(first_slot + i * wb) * kTileM));
+  const float m0 = mx == -INFINITY ? 0.f : mx;
+  float sum = 0.f;
+  for (int i = 0; i < np; ++i) sum += exp2f(__ldcg(plse + (size_t)(first_slot + i * wb) * kTileM) - m0);
+  const float lse2 = sum > 0.f ? m0 + log2f(sum) : -INFINITY;
+  const size_t orow = (size_t)(w / Qb) * rows_q + flat;
+  if (t < 64 && p.lse) p.lse[orow] = lse2 * 0.69314718055994530942f;
+#pragma unroll 1
+  for (int cb = t >> 6; cb < kDLatent / 32; cb += nthr >> 6) {
+    const int d0 = 32 * cb;
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll 1
+    for (int i0 = 0; i0 < np; i0 += 2) {
+      float x[2][32];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint8_t* so = part_o + (size_t)(first_slot + min(i0 + u, np - 1) * wb) * slot_bytes;
+        if (p.partial_f16) {
+          const uint4* src = reinterpret_cast<const uint4*>(so) + m;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldcg(src + (size_t)(d0 / 8 + q) * kTileM);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+              x[u][8 * q + 2 * e] = f.x;
+              x[u][8 * q + 2 * e + 1] = f.y;
+            }
+          }
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(so) + m;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 v = __ldcg(src + (size_t)(d0 / 4 + q) * kTileM);
+            x[u][4 * q] = v.x;
+            x[u][4 * q + 1] = v.y;
+            x[u][4 * q + 2] = v.z;
+            x[u][4 * q + 3] = v.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float li = i0 + u < np ? __ldcg(plse + (size_t)(first_slot + (i0 + u) * wb) * kTileM) : -INFINITY;
+        if (!(sum > 0.f) || li == -INFINITY) continue;
+        const float wt = exp2f(li - lse2) * p.ckv_descale;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] += wt * x[u][e];
+      }
+    }
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDLatent + d0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    } else {
+      uint32_t r[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(acc[e]);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * kDLatent + d0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = pack8_bf16(r + 8 * q, 1.f);
+    }
+  }
+}
+
+// Fused combine: the work rows with no visible key in any of their M rows have no piece;
+// this CTA's share of them (every gridDim.x-th) gets O = 0 and LSE = -inf (the correction
+// warps, 128 threads, one M row each).  Out of line: once per kernel.
+__device__ __noinline__ void write_empty_rows(const DecodeParams& p, const DealShape& DS, int L) {
+  const int rows_q = p.Sq * p.H;
+  for (int w = blockIdx.x; w < DS.Rw; w += gridDim.x) {
+    const int b = w / DS.Qb, i = w % DS.Qb;
+    const int K = clamp_len(p, b, nullptr);
+    int tlo, n;
+    work_span(p, b, i, K, global_len(p, b, K), tlo, n);
+    if (n > 0) continue;
+    const int flat = kTileM * i + L;
+    if (flat >= rows_q) continue;
+    const size_t orow = (size_t)b * rows_q + flat;
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDLatent);
+      for (int q = 0; q < kDLatent / 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * kDLatent);
+      for (int q = 0; q < kDLatent / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+    }
+    if (p.lse) p.lse[orow] = -INFINITY;
+  }
+}
+
 // Epilogue of one piece for this thread's M row (correction warps, once per piece): a
 // work row in one piece goes to the output (O / l times the value scale, natural-log
 // LSE); a piece of a longer row goes to its slot (O / l in the stored codes' units and
@@ -380,6 +532,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 10; ++i) M.nfill[i] = M.fbytes[i] = 0;
     M.ntail[0] = M.ntail[1] = M.ntail_done[0] = M.ntail_done[1] = 0;
     M.nq = 0;
+    M.ncl = 0;
   }
   __syncthreads();
   {
@@ -412,6 +565,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&M.tail_bar[1]), 1);
     mbar_init(smem_addr(&M.xchg_bar), 4);
     mbar_init(smem_addr(&M.drain), 1);
+    mbar_init(smem_addr(&M.comb_in), 4);
+    mbar_init(smem_addr(&M.comb_out), 1);
     fence_mbar_init();
   }
   if (warp == 8) {
@@ -626,6 +781,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t obase = tmem + lanebase + 256;
     const int m = 64 * (int)rank + row;  // this thread's M row
     int j = 0;
+    uint32_t ncomb = 0;  // fused combines so far (the parity of their syncs)
     bool ok = true;
     for (int s = 0; s < nseg && ok; ++s) {
       const Segment sg = seg_at(s);
@@ -669,8 +825,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       piece_epilogue(p, p.ws + WL.partial_o + sl * WL.slot_bytes,
                      reinterpret_cast<float*>(p.ws + WL.partial_lse) + sl * kTileM, obase, half, m, b, flat,
                      flat < rows_q, slot < 0, M.fin_l[s & 1][L], M.fin_m[s & 1][L]);
+      if (p.fused_combine && slot >= 0) {
+        tc_fence_before();
+        const int first = slot - sg.piece() * DS.wb;
+        const int v = arrive_piece(M, p,
+                                   reinterpret_cast<unsigned long long*>(p.ws + WL.counters) + 2 * (size_t)sg.row() + rank,
+                                   ncomb & 1, sg.row(), first, sg.n_parts(), L);
+        ++ncomb;
+        if (!(ok = v >= 0)) break;
+        if (v > 0)
+          combine_row(p, p.ws + WL.partial_o, reinterpret_cast<const float*>(p.ws + WL.partial_lse), WL.slot_bytes,
+                      sg.row(), first, sg.n_parts(), DS.wb, DS.Qb, rank, L, 128);
+      }
       tc_fence_before();
     }
+    if (ok && p.fused_combine) write_empty_rows(p, DS, L);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue (leader CTA)
     if (rank == 0 && lane == 0) {
@@ -970,6 +1139,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == 8) tmem_dealloc_pair(tmem, 512);
   if (tid == 0) reinterpret_cast<uint32_t*>(p.ws + WL.cta_status)[2 * cl + rank] = M.err;
+  // the work rows this CTA arrived last on, by 8 warps (no abort: every piece arrived)
+  if (p.fused_combine && !*reinterpret_cast<volatile uint32_t*>(&M.abort) && tid < 256) {
+    const int n = min((int)M.ncl, kCombList);
+    for (int e = 0; e < n; ++e) {
+      const int4 E = M.comb_list[e];
+      combine_row(p, p.ws + WL.partial_o, reinterpret_cast<const float*>(p.ws + WL.partial_lse), WL.slot_bytes, E.x,
+                  E.y, E.z, DS.wb, DS.Qb, rank, tid, 256);
+    }
+  }
 }
 
 }  // namespace tc

@@ -224,6 +224,7 @@ __device__ __forceinline__ int build_segments(const DecodeParams& p, const Sched
           sg.tile_begin = t_begin;
           sg.tile_end = t_end;
           sg.K = K;
+          sg.parts = (uint32_t)np | ((uint32_t)(g - g_first) << 16);
           has = true;
         }
       }

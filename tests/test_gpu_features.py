@@ -5,7 +5,9 @@
   local bounds     per-token local_visible_lens (the page's __call__)
   context parallel each rank's share of every row (cp_world, cp_rank, cp_interleave_size,
                    causal_seqs), merged on the GPU with mla_merge
-  fp16 partials    partial_fp16, reducer D bands (reducer_d_tiles), programmatic dependent launch
+  combining        rows cut into pieces combined by the reduction kernel, or in the split-KV
+                   kernel by their last piece (combine_in_kernel): fp16 or fp32 partials
+                   (partial_fp16), reducer D bands (reducer_d_tiles), programmatic dependent launch
 
 Tolerances as in test_gpu_parity: bf16 max|O - O*| <= 1e-2 max|O*|, |LSE - LSE*| <= 1e-3;
 e4m3 5e-2 and 2e-2.
@@ -198,13 +200,41 @@ def test_merge_of_empty_and_single_pieces():
 
 
 # ---------------------------------------------------------------- fp16 partials, reducer bands, PDL
-@pytest.mark.parametrize("opts", [dict(partial_fp16=True), dict(partial_fp16=True, reducer_d_tiles=1),
+@pytest.mark.parametrize("opts", [dict(combine_in_kernel=True, partial_fp16=True),
+                                  dict(combine_in_kernel=True, partial_fp16=False),
+                                  dict(partial_fp16=True), dict(partial_fp16=True, reducer_d_tiles=1),
                                   dict(reducer_d_tiles=2), dict(reducer_d_tiles=4, use_pdl=True),
                                   dict(partial_fp16=True, use_pdl=True)])
 def test_partial_formats_and_reducer_bands(opts):
     prob = wl.make_problem("uniform", seed=505, H=128, Sq=2, causal=True, seq_lens=[5000, 300, 2048, 9, 0])
     O, L = host(*run(prob, num_clusters=40, **opts))
     compare("bf16", O, L, *oracle.decode(prob.host_inputs()))
+
+
+def test_combine_in_kernel_reuses_one_workspace_across_calls_and_shapes():
+    """Rows cut into many pieces, combined by their last piece: one workspace, zeroed once,
+    serves repeated calls and plans of other shapes (the arrival counters carry each call's
+    tag), and agrees with the separate reduction kernel."""
+    p1 = wl.make_problem("uniform", seed=71, H=128, Sq=2, causal=True, seq_lens=[5000, 300, 2048, 9, 0])
+    p2 = wl.make_problem("uniform", seed=72, H=64, Sq=3, causal=True, seq_lens=[7000, 1, 4000, 640])
+    d1 = decoder_for(p1, num_clusters=40, combine_in_kernel=True)
+    d2 = decoder_for(p2, num_clusters=24, combine_in_kernel=True)
+    shared = torch.zeros(max(d1.workspace.numel(), d2.workspace.numel()), dtype=torch.uint8, device="cuda")
+    d1.workspace = d2.workspace = shared
+    ref1, ref2 = oracle.decode(p1.host_inputs()), oracle.decode(p2.host_inputs())
+    i1, i2 = p1.device_inputs("cuda"), p2.device_inputs("cuda")
+    for prob, dec, d, ref in [(p1, d1, i1, ref1), (p2, d2, i2, ref2), (p1, d1, i1, ref1), (p2, d2, i2, ref2),
+                              (p2, d2, i2, ref2)]:
+        out, lse = dec(d["q_latent"], d["q_rope"], d["ckv"], d["kpe"], d["page_table"], d["seq_lens"], d["scale"])
+        torch.cuda.synchronize()
+        assert dec.status() == n.MLA_OK
+        compare("bf16", *host(out, lse), *ref)
+    o_red, l_red = run(p1, d=i1, num_clusters=40)
+    o_fused, l_fused = run(p1, d=i1, num_clusters=40, combine_in_kernel=True)
+    assert torch.allclose(o_fused.float(), o_red.float(), rtol=2e-2, atol=2e-3 * o_red.float().abs().max().item())
+    fin = torch.isfinite(l_red)
+    assert torch.equal(fin, torch.isfinite(l_fused))
+    assert torch.allclose(l_fused[fin], l_red[fin], rtol=0, atol=1e-4)
 
 
 def test_fp16_partials_e4m3_full_size():
