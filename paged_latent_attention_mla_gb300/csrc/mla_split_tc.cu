@@ -786,10 +786,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < nseg && ok; ++s) {
       const Segment sg = seg_at(s);
       const int n = sg.tile_end - sg.tile_begin;
+      float fl = 0.f, fm = 0.f;  // the piece's final row statistics
       for (int i = 0; i < n; ++i, ++j) {
         const int st = j & 1;
         if (!(ok = kwait(M, smem_addr(&M.cor_ready[st]), (j >> 1) & 1))) break;
         const float fac = M.corr[st][L];
+        if (i == n - 1) {
+          // read before this tile's arrival below: the softmax can then run at most two
+          // tiles ahead, and writes these statistics again only for the piece after next
+          fl = M.fin_l[s & 1][L];
+          fm = M.fin_m[s & 1][L];
+        }
         if (i > 0 && __any_sync(0xffffffffu, fac != 1.f)) {
           // O holds tiles < j once the P.V of tile j - 1 completes
           if (!(ok = kwait(M, smem_addr(&M.o_done[st ^ 1]), ((j - 1) >> 1) & 1))) break;
@@ -824,7 +831,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const size_t sl = slot < 0 ? 0 : (size_t)slot;
       piece_epilogue(p, p.ws + WL.partial_o + sl * WL.slot_bytes,
                      reinterpret_cast<float*>(p.ws + WL.partial_lse) + sl * kTileM, obase, half, m, b, flat,
-                     flat < rows_q, slot < 0, M.fin_l[s & 1][L], M.fin_m[s & 1][L]);
+                     flat < rows_q, slot < 0, fl, fm);
       if (p.fused_combine && slot >= 0) {
         tc_fence_before();
         const int first = slot - sg.piece() * DS.wb;
@@ -832,7 +839,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                    reinterpret_cast<unsigned long long*>(p.ws + WL.counters) + 2 * (size_t)sg.row() + rank,
                                    ncomb & 1, sg.row(), first, sg.n_parts(), L);
         ++ncomb;
-        if (!(ok = v >= 0)) break;
+        ok = v >= 0;
+        if (!ok) break;
         if (v > 0)
           combine_row(p, p.ws + WL.partial_o, reinterpret_cast<const float*>(p.ws + WL.partial_lse), WL.slot_bytes,
                       sg.row(), first, sg.n_parts(), DS.wb, DS.Qb, rank, L, 128);
@@ -846,7 +854,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int j = 0, pvc = 0, tcount = 0;
       int rslot = 0;        // next ring slot in consumption order
       uint32_t rphase = 0;  // and the parity of its fill
-      int ngroups = 0, tail_rows = 0;  // of the current piece's request
       bool ok = true;
       // next ring slot: wait until both CTAs' copies landed (one CTA-scope test in the
       // common case, the bounded wait otherwise)
@@ -890,7 +897,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mma_commit_pair(smem_addr(&M.s_full[st]), 0x3);
         return true;
       };
-      auto pv = [&](bool first, int tile) -> bool {
+      // P.V of tile `tile` of a request with ngroups key groups, the last tail_rows long
+      auto pv = [&](bool first, int tile, int ngroups, int tail_rows) -> bool {
         const int pst = pvc & 1;
         if (!kwait(M, smem_addr(&M.pv_ready[pst]), (pvc >> 1) & 1)) return false;
         tc_fence_after();
@@ -928,11 +936,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++pvc;
         return true;
       };
+      // One software pipeline over the CTA's tiles, across pieces: QK^T(t + 1) then P.V(t),
+      // also when t + 1 opens the next piece (the ring holds K(t + 1) ahead of V(t))
+      bool pend = false, pend_first = false;  // the tile whose P.V is still to be issued
+      int pend_tile = 0, pend_ng = 0, pend_tr = 0;
       for (int s = 0; s < nseg && ok; ++s) {
         const Segment sg = seg_at(s);
         const int n = sg.tile_end - sg.tile_begin;
-        ngroups = cdiv(sg.K, kKeyGroup);
-        tail_rows = sg.K % kKeyGroup;
+        const int ng = cdiv(sg.K, kKeyGroup), tr = sg.K % kKeyGroup;
         if (!(ok = kwait(M, smem_addr(&M.q_full), s & 1))) break;
         tc_fence_after();
         for (int i = 0; i < n && ok; ++i) {
@@ -940,28 +951,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // Q is free once the piece's last QK^T completes: the next piece's Q load need
           // not wait for the P.V issued after it
           if (ok && i == n - 1) mma_commit_pair(smem_addr(&M.q_empty), 0x3);
-          if (ok && i >= 1) ok = pv(i == 1, sg.tile_begin + i - 1);
+          if (ok && pend) ok = pv(pend_first, pend_tile, pend_ng, pend_tr);
+          pend = true;
+          pend_first = i == 0;
+          pend_tile = sg.tile_begin + i;
+          pend_ng = ng;
+          pend_tr = tr;
         }
-        if (!ok) break;
-        ok = pv(n == 1, sg.tile_end - 1);
         j += n;
       }
+      if (ok && pend) ok = pv(pend_first, pend_tile, pend_ng, pend_tr);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ Q loads
-    if (lane == 0) {
-      for (int s = 0; s < nseg; ++s) {
-        if (s > 0 && !kwait(M, smem_addr(&M.q_empty), (s - 1) & 1)) break;
-        const uint32_t bar = lead(M.q_full);
-        // the leader arms the barrier with both CTAs' bytes; the peer's copies only complete bytes on it
-        if (rank == 0) mbar_arrive_expect_tx(smem_addr(&M.q_full), 2 * C::kQBytes);
-        const int wr = seg_at(s).row(), b = wr / DS.Qb;
-        const int r0 = kTileM * (wr % DS.Qb) + 64 * (int)rank;  // this CTA's 64 (token, head) rows
-        for (int kb = 0; kb < C::kNLat; ++kb)
-          tma_load_3d_pair(sQ + kb * 8192, &maps.q_latent, kb * C::kBlk, r0, b, bar);
-        tma_load_3d_pair(sQ + C::kNLat * 8192, &maps.q_rope, 0, r0, b, bar);
-        M.nq = s + 1;
-      }
+    // lane kb issues Q block kb (one copy a lane: a thread's copies go out one after another);
+    // lane 0 waits and the warp follows its verdict, so the count of issued loads is exact
+    for (int s = 0; s < nseg; ++s) {
+      bool okq = true;
+      if (s > 0 && lane == 0) okq = kwait(M, smem_addr(&M.q_empty), (s - 1) & 1);
+      if (!__shfl_sync(0xffffffffu, okq ? 1 : 0, 0)) break;
+      const uint32_t bar = lead(M.q_full);
+      // the leader arms the barrier with both CTAs' bytes; the peer's copies only complete bytes on it
+      if (lane == 0 && rank == 0) mbar_arrive_expect_tx(smem_addr(&M.q_full), 2 * C::kQBytes);
+      const int wr = seg_at(s).row(), b = wr / DS.Qb;
+      const int r0 = kTileM * (wr % DS.Qb) + 64 * (int)rank;  // this CTA's 64 (token, head) rows
+      if (lane < C::kNLat) tma_load_3d_pair(sQ + lane * 8192, &maps.q_latent, lane * C::kBlk, r0, b, bar);
+      else if (lane == C::kNLat) tma_load_3d_pair(sQ + C::kNLat * 8192, &maps.q_rope, 0, r0, b, bar);
+      if (lane == 0) M.nq = s + 1;
+      __syncwarp();
     }
   } else if (warp >= 10) {
     // ------------------------------------------------------------ K blocks and V key groups, one ring
@@ -996,134 +1013,166 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     struct TileBoxes {
       int pg[4], rw[4];
     };
+    bool bad_page = false;
+    auto fetch = [&](int b, int K, int tile, TileBoxes& tb) {
+      bool bad;
+      if constexpr (one_box) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          box_page(p.page_table, p.pt_stride, p.num_pages, p.page_shift, b, tile * kTileN + q * kKeyGroup, K, tb.pg[q],
+                   tb.rw[q], bad);
+          bad_page |= bad;
+        }
+      } else if (lane < 4 * nb) {
+        box_page(p.page_table, p.pt_stride, p.num_pages, p.page_shift, b, tile * kTileN + lane * br, K, tb.pg[0],
+                 tb.rw[0], bad);
+        bad_page |= bad;
+      } else {
+        tb.pg[0] = p.num_pages;
+      }
+    };
+    // below 64: this lane's box of the tile into the warp's table, at the loader's tile
+    // count ti mod 3 (the tile whose V is loaded, the one whose K is loaded, the next)
+    auto publish = [&](int ti, const TileBoxes& tb) {
+      if constexpr (one_box) return;
+      table[(ti % 3) * 32 + lane] = tb.pg[0];
+      __syncwarp();
+    };
+    // page and row of box k (k < 4 nb) of a tile, in the issuing lane
+    auto box = [&](const TileBoxes& tb, int ti, int k, int& pg, int& rw) {
+      if constexpr (one_box) {
+        // selects, not a runtime index: the boxes stay in registers
+        pg = k == 0 ? tb.pg[0] : k == 1 ? tb.pg[1] : k == 2 ? tb.pg[2] : tb.pg[3];
+        rw = k == 0 ? tb.rw[0] : k == 1 ? tb.rw[1] : k == 2 ? tb.rw[2] : tb.rw[3];
+      } else {
+        pg = table[(ti % 3) * 32 + k];
+        rw = 0;
+      }
+    };
+    auto load_k = [&](int ti, const TileBoxes& tb) -> bool {
+      for (int kb = 0; kb < C::kNKb; ++kb) {
+        int slot;
+        bool mine;
+        if (!acquire(slot, mine)) return false;
+        if (mine && lane < 2 * nb) {
+          // lane q issues box q of the fill: a thread's copies go out one after another, so
+          // the fill's boxes leave from separate lanes
+          const bool rope = kb == C::kNLat;
+          const int rowb = rope ? C::kRopeRow : 128;  // bytes per key row of the block
+          const uint32_t bar = lead(M.full[slot]);
+          const uint32_t dst = sRing + slot * C::kSlot;
+          // both CTAs' two key groups
+          if (lane == 0 && rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot]), 4 * 64 * rowb);
+          const int k0 = 2 * (int)rank * nb;  // this CTA's boxes: key groups 2 rank, 2 rank + 1
+          int pg, rw;
+          box(tb, ti, k0 + lane, pg, rw);
+          const uint32_t d = dst + lane * br * rowb;
+          if (!rope) tma_load_3d_pair(d, &maps.ckv, kb * C::kBlk, rw, pg, bar);
+          else tma_load_3d_pair(d, &maps.kpe, 0, rw, pg, bar);
+          if (lane == 0) {
+            M.nfill[slot] += 1;
+            M.fbytes[slot] = 2 * 64 * rowb;
+          }
+        }
+        __syncwarp();
+      }
+      return true;
+    };
+    // V of tile `tile` of a request with ngroups key groups, the last tail_rows long (0: full)
+    auto load_v = [&](int tile, int ti, int ngroups, int tail_rows, const TileBoxes& tb) -> bool {
+      for (int vp = 0; vp < 4; ++vp) {
+        int slot[2];
+        bool mine[2];
+        int nmine = 0;
+#pragma unroll
+        for (int it = 0; it < C::kVItems; ++it) {
+          if (!acquire(slot[it], mine[it])) return false;
+          nmine += mine[it] ? 1 : 0;
+        }
+        const bool tail = 4 * tile + vp == ngroups - 1 && tail_rows != 0 && nmine != 0;
+        // this CTA's 128-byte column blocks of V: bf16 blocks {0,1,4,5} or {2,3,6,7}
+        // (two per slot, one slot per output chunk), e4m3 blocks {rank, 2 + rank}
+        const uint32_t tbar = smem_addr(&M.tail_bar[own]);
+        if (lane < 2 * nb) {
+          // lane 2 q + u issues page box q of column block u (see load_k: one box a lane)
+          if (tail && lane == 0) mbar_arrive_expect_tx(tbar, nmine * C::kSlot);
+          const int q = lane >> 1, u = lane & 1;
+#pragma unroll
+          for (int it = 0; it < C::kVItems; ++it) {
+            if (!mine[it]) continue;
+            const uint32_t dst = sRing + slot[it] * C::kSlot;
+            const uint32_t bar = lead(M.full[slot[it]]);
+            if (!tail && lane == 0 && rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot[it]]), 2 * C::kSlot);
+            int pg, rw;
+            box(tb, ti, vp * nb + q, pg, rw);
+            const int gb = E4M3 ? 2 * u + (int)rank : 4 * it + 2 * (int)rank + u;
+            const uint32_t d = dst + u * 8192 + q * br * 128;
+            if (tail) tma_load_3d(d, &maps.ckv, gb * C::kBlk, rw, pg, tbar);
+            else tma_load_3d_pair(d, &maps.ckv, gb * C::kBlk, rw, pg, bar);
+            if (lane == 0) {
+              M.nfill[slot[it]] += 1;
+              M.fbytes[slot[it]] = tail ? 0u : (uint32_t)C::kSlot;
+            }
+          }
+          if (tail && lane == 0) M.ntail[own] += 1;
+        }
+        __syncwarp();
+        if (tail) {
+          if (!tail_group<E4M3>(M, smem, own, rank, lane, tph, slot[0], slot[C::kVItems - 1], mine[0],
+                                mine[C::kVItems - 1], tail_rows))
+            return false;
+          ++tph;
+        }
+      }
+      return true;
+    };
+    // e4m3, page size >= 64: this CTA's K rows of a tile (its two key groups, latent and
+    // rope: each a page's contiguous rows) prefetched into L2 a tile ahead of their copies
+    // (measured: shorter e4m3 launches, slightly longer bf16 ones)
+    auto prefetch_k = [&](const TileBoxes& tb) {
+      if constexpr (one_box && E4M3) {
+        if (own == 0 && lane < 4) {
+          int pg, rw;
+          box(tb, 0, 2 * (int)rank + (lane & 1), pg, rw);
+          if (pg < p.num_pages) {
+            const bool rope = lane >= 2;
+            const size_t rb = (size_t)(rope ? kDRope : kDLatent) * (E4M3 ? 1 : 2);  // bytes per key row
+            const uint8_t* base = static_cast<const uint8_t*>(rope ? p.kpe : p.ckv);
+            prefetch_l2_bulk(base + ((size_t)pg * p.page_size + rw) * rb, (uint32_t)(kKeyGroup * rb));
+          }
+        }
+      }
+    };
+    // One software pipeline over the CTA's tiles, across pieces: K(t + 1) goes ahead of V(t)
+    // also when t + 1 opens the next piece, so a piece's last P.V never drains the ring
+    bool pend = false;  // the tile whose V is still to be loaded
+    int pend_tile = 0, pend_ti = 0, pend_ng = 0, pend_tr = 0;
+    TileBoxes pend_tb;
+    int ti = 0;  // tiles of this CTA so far
     for (int s = 0; s < nseg && ok; ++s) {
       const Segment sg = seg_at(s);
       const int b = sg.row() / DS.Qb;
       const int K = sg.K;
-      const int ngroups = cdiv(K, kKeyGroup);
-      const int tail_rows = K % kKeyGroup;
-      bool bad_page = false;
-      auto fetch = [&](int tile, TileBoxes& tb) {
-        bool bad;
-        if constexpr (one_box) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            box_page(p.page_table, p.pt_stride, p.num_pages, p.page_shift, b, tile * kTileN + q * kKeyGroup, K,
-                     tb.pg[q], tb.rw[q], bad);
-            bad_page |= bad;
-          }
-        } else if (lane < 4 * nb) {
-          box_page(p.page_table, p.pt_stride, p.num_pages, p.page_shift, b, tile * kTileN + lane * br, K, tb.pg[0],
-                   tb.rw[0], bad);
-          bad_page |= bad;
-        } else {
-          tb.pg[0] = p.num_pages;
-        }
-      };
-      // below 64: this lane's box of the tile into the warp's table (three tiles in use)
-      auto publish = [&](int tile, const TileBoxes& tb) {
-        if constexpr (one_box) return;
-        table[(tile % 3) * 32 + lane] = tb.pg[0];
-        __syncwarp();
-      };
-      // page and row of box k (k < 4 nb) of a tile, in the issuing lane
-      auto box = [&](const TileBoxes& tb, int tile, int k, int& pg, int& rw) {
-        if constexpr (one_box) {
-          // selects, not a runtime index: the boxes stay in registers
-          pg = k == 0 ? tb.pg[0] : k == 1 ? tb.pg[1] : k == 2 ? tb.pg[2] : tb.pg[3];
-          rw = k == 0 ? tb.rw[0] : k == 1 ? tb.rw[1] : k == 2 ? tb.rw[2] : tb.rw[3];
-        } else {
-          pg = table[(tile % 3) * 32 + k];
-          rw = 0;
-        }
-      };
-      auto load_k = [&](int tile, const TileBoxes& tb) -> bool {
-        for (int kb = 0; kb < C::kNKb; ++kb) {
-          int slot;
-          bool mine;
-          if (!acquire(slot, mine)) return false;
-          if (mine && lane == 0) {
-            const bool rope = kb == C::kNLat;
-            const int rowb = rope ? C::kRopeRow : 128;  // bytes per key row of the block
-            const uint32_t bar = lead(M.full[slot]);
-            const uint32_t dst = sRing + slot * C::kSlot;
-            // both CTAs' two key groups
-            if (rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot]), 4 * 64 * rowb);
-            const int k0 = 2 * (int)rank * nb;  // this CTA's boxes: key groups 2 rank, 2 rank + 1
-            for (int q = 0; q < 2 * nb; ++q) {
-              int pg, rw;
-              box(tb, tile, k0 + q, pg, rw);
-              const uint32_t d = dst + q * br * rowb;
-              if (!rope) tma_load_3d_pair(d, &maps.ckv, kb * C::kBlk, rw, pg, bar);
-              else tma_load_3d_pair(d, &maps.kpe, 0, rw, pg, bar);
-            }
-            M.nfill[slot] += 1;
-            M.fbytes[slot] = 2 * 64 * rowb;
-          }
-          __syncwarp();
-        }
-        return true;
-      };
-      auto load_v = [&](int tile, const TileBoxes& tb) -> bool {
-        for (int vp = 0; vp < 4; ++vp) {
-          int slot[2];
-          bool mine[2];
-          int nmine = 0;
-#pragma unroll
-          for (int it = 0; it < C::kVItems; ++it) {
-            if (!acquire(slot[it], mine[it])) return false;
-            nmine += mine[it] ? 1 : 0;
-          }
-          const bool tail = 4 * tile + vp == ngroups - 1 && tail_rows != 0 && nmine != 0;
-          // this CTA's 128-byte column blocks of V: bf16 blocks {0,1,4,5} or {2,3,6,7}
-          // (two per slot, one slot per output chunk), e4m3 blocks {rank, 2 + rank}
-          const uint32_t tbar = smem_addr(&M.tail_bar[own]);
-          if (lane == 0) {
-            if (tail) mbar_arrive_expect_tx(tbar, nmine * C::kSlot);
-#pragma unroll
-            for (int it = 0; it < C::kVItems; ++it) {
-              if (!mine[it]) continue;
-              const uint32_t dst = sRing + slot[it] * C::kSlot;
-              const uint32_t bar = lead(M.full[slot[it]]);
-              if (!tail && rank == 0) mbar_arrive_expect_tx(smem_addr(&M.full[slot[it]]), 2 * C::kSlot);
-              for (int q = 0; q < nb; ++q) {
-                int pg, rw;
-                box(tb, tile, vp * nb + q, pg, rw);
-                for (int u = 0; u < 2; ++u) {
-                  const int gb = E4M3 ? 2 * u + (int)rank : 4 * it + 2 * (int)rank + u;
-                  const uint32_t d = dst + u * 8192 + q * br * 128;
-                  if (tail) tma_load_3d(d, &maps.ckv, gb * C::kBlk, rw, pg, tbar);
-                  else tma_load_3d_pair(d, &maps.ckv, gb * C::kBlk, rw, pg, bar);
-                }
-              }
-              M.nfill[slot[it]] += 1;
-              M.fbytes[slot[it]] = tail ? 0u : (uint32_t)C::kSlot;
-            }
-            if (tail) M.ntail[own] += 1;
-          }
-          __syncwarp();
-          if (tail) {
-            if (!tail_group<E4M3>(M, smem, own, rank, lane, tph, slot[0], slot[C::kVItems - 1], mine[0],
-                                  mine[C::kVItems - 1], tail_rows))
-              return false;
-            ++tph;
-          }
-        }
-        return true;
-      };
-      TileBoxes prev, cur, next;
-      fetch(sg.tile_begin, cur);
-      for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile) {
-        if (tile + 1 < sg.tile_end) fetch(tile + 1, next);  // read a tile ahead
-        publish(tile, cur);
-        ok = load_k(tile, cur);
-        if (ok && tile > sg.tile_begin) ok = load_v(tile - 1, prev);
-        prev = cur;
+      const int ng = cdiv(K, kKeyGroup), tr = K % kKeyGroup;
+      TileBoxes cur, next;
+      fetch(b, K, sg.tile_begin, cur);
+      for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile, ++ti) {
+        if (tile + 1 < sg.tile_end) fetch(b, K, tile + 1, next);  // read a tile ahead
+        publish(ti, cur);
+        ok = load_k(ti, cur);
+        if (ok && tile + 1 < sg.tile_end) prefetch_k(next);
+        if (ok && pend) ok = load_v(pend_tile, pend_ti, pend_ng, pend_tr, pend_tb);
+        pend = true;
+        pend_tile = tile;
+        pend_ti = ti;
+        pend_ng = ng;
+        pend_tr = tr;
+        pend_tb = cur;
         cur = next;
       }
-      if (ok) ok = load_v(sg.tile_end - 1, prev);
-      if (__any_sync(0xffffffffu, bad_page) && own == 0 && lane == 0) atomicOr(&M.err, kErrBadPage);
     }
+    if (ok && pend) ok = load_v(pend_tile, pend_ti, pend_ng, pend_tr, pend_tb);
+    if (__any_sync(0xffffffffu, bad_page) && own == 0 && lane == 0) atomicOr(&M.err, kErrBadPage);
   }
 
   // ------------------------------------------------------------ teardown
