@@ -233,6 +233,8 @@ def decode_options(args, prob) -> dict:
     """Decoder options the run asks for: the wrapper's defaults (PDL reduction, fp16 partials
     for e4m3) unless told otherwise."""
     opts = {"use_pdl": not args.no_pdl, "combine_in_kernel": args.combine_in_kernel}
+    if args.num_clusters:
+        opts["num_clusters"] = args.num_clusters
     if args.partial_fp16:
         opts["partial_fp16"] = True
     return opts
@@ -435,6 +437,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
     ap.add_argument("--partial-fp16", action="store_true", help="fp16 split partials for bf16 caches too")
+    ap.add_argument("--num-clusters", type=int, default=0, help="CTA pairs of the split-KV launch (0: the planner's)")
     ap.add_argument("--no-pdl", action="store_true", help="launch the reduction without programmatic dependent launch")
     ap.add_argument("--combine-in-kernel", action="store_true",
                     help="combine split rows inside the split-KV kernel instead of in the reduction kernel")

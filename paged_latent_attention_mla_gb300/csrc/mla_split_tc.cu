@@ -533,20 +533,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     M.ntail[0] = M.ntail[1] = M.ntail_done[0] = M.ntail_done[1] = 0;
     M.nq = 0;
     M.ncl = 0;
-  }
-  __syncthreads();
-  {
-    // the batch schedule, in the ring memory before any tile lands there
-    int32_t* scratch = reinterpret_cast<int32_t*>(smem + C::kOffRing);
-    Sched sc = build_schedule(p, scratch, &M.err);
-    if (blockIdx.x * blockDim.x < DS.Rw) write_row_table(p, sc);  // the CTAs that own rows of the table
-    if (warp == 0) {
-      const int nseg = build_segments(p, sc, cl, segs, overflow);
-      if (lane == 0) M.nseg = nseg;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
     mbar_init(smem_addr(&M.q_full), 1);  // armed by the leader with both CTAs' bytes
     mbar_init(smem_addr(&M.q_empty), 1);
     for (int i = 0; i < C::kNS; ++i) {
@@ -569,6 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&M.comb_out), 1);
     fence_mbar_init();
   }
+  // what needs no schedule goes first: the barriers above, tensor memory, the descriptors
   if (warp == 8) {
     tmem_alloc_pair(smem_addr(&M.tmem_base), 512);
     tmem_relinquish_pair();
@@ -579,6 +566,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&maps.q_latent);
     tma_prefetch_desc(&maps.q_rope);
   }
+  __syncthreads();
+  {
+    // the batch schedule, in the ring memory before any tile lands there
+    int32_t* scratch = reinterpret_cast<int32_t*>(smem + C::kOffRing);
+    Sched sc = build_schedule(p, scratch, &M.err);
+    if (blockIdx.x * blockDim.x < DS.Rw) write_row_table(p, sc);  // the CTAs that own rows of the table
+    if (warp == 0) {
+      const int nseg = build_segments(p, sc, cl, segs, overflow);
+      if (lane == 0) M.nseg = nseg;
+    }
+  }
+  __syncthreads();
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
