@@ -44,6 +44,42 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
   const float* plse = reinterpret_cast<const float*>(p.ws + L.partial_lse) + m;
   const uint8_t* po = p.ws + L.partial_o;
   auto slot_of = [&](int i) { return (size_t)ri.first_slot + (size_t)i * d.wb; };
+  // 32 dims of piece i from d0 into x
+  auto load = [&](int i, int d0, float (&x)[32]) {
+    const size_t sl = slot_of(i);
+    if constexpr (F16) {
+      const uint4* src = reinterpret_cast<const uint4*>(po + sl * L.slot_bytes) + m;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldcs(src + (size_t)(d0 / 8 + q) * kTileM);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+          x[8 * q + 2 * e] = f.x;
+          x[8 * q + 2 * e + 1] = f.y;
+        }
+      }
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(po + sl * L.slot_bytes) + m;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 v = __ldcs(src + (size_t)(d0 / 4 + q) * kTileM);
+        x[4 * q] = v.x;
+        x[4 * q + 1] = v.y;
+        x[4 * q + 2] = v.z;
+        x[4 * q + 3] = v.w;
+      }
+    }
+  };
+  const int band = kDLatent / p.reduce_d_tiles;
+  // the first round's partials (pieces 0 and 1 of the first chunk) go out with the LSE
+  // loads, before the LSE arithmetic: one dependent round trip fewer
+  float x[2][32];
+  if (np > 0) {
+    load(0, blockIdx.x * band + 32 * dg, x[0]);
+    load(np > 1 ? 1 : 0, blockIdx.x * band + 32 * dg, x[1]);
+  }
   // the pieces' LSEs: max, sum, the row's LSE
   float mx = -INFINITY;
   for (int i = 0; i < np; ++i) mx = fmaxf(mx, plse[slot_of(i) * kTileM]);
@@ -55,7 +91,6 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
     const float li = plse[slot_of(i) * kTileM];
     return (sum > 0.f && li != -INFINITY) ? exp2f(li - lse2) * p.ckv_descale : 0.f;
   };
-  const int band = kDLatent / p.reduce_d_tiles;
   for (int c = 0; c < band / 64; ++c) {
     const int d0 = blockIdx.x * band + 64 * c + 32 * dg;  // this thread's 32 dims
     float acc[32];
@@ -64,34 +99,9 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
     // two pieces per round, both rounds' loads issued before their weights are applied;
     // an empty piece (LSE -inf) gets weight 0 and is selected away
     for (int i0 = 0; i0 < np; i0 += 2) {
-      float x[2][32];
+      if (c > 0 || i0 > 0) {
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const size_t sl = slot_of(i0 + u < np ? i0 + u : i0);
-        if constexpr (F16) {
-          const uint4* src = reinterpret_cast<const uint4*>(po + sl * L.slot_bytes) + m;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = __ldcs(src + (size_t)(d0 / 8 + q) * kTileM);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-              x[u][8 * q + 2 * e] = f.x;
-              x[u][8 * q + 2 * e + 1] = f.y;
-            }
-          }
-        } else {
-          const float4* src = reinterpret_cast<const float4*>(po + sl * L.slot_bytes) + m;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 v = __ldcs(src + (size_t)(d0 / 4 + q) * kTileM);
-            x[u][4 * q] = v.x;
-            x[u][4 * q + 1] = v.y;
-            x[u][4 * q + 2] = v.z;
-            x[u][4 * q + 3] = v.w;
-          }
-        }
+        for (int u = 0; u < 2; ++u) load(i0 + u < np ? i0 + u : i0, d0, x[u]);
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
