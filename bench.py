@@ -49,10 +49,10 @@ ALL = ["uniform", "varlen", "fp8spec", "window"]
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 321493504 + 14273792},
-    "varlen": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 554160896 + 19035904},
-    "fp8spec": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 310223360 + 8945664},
-    "window": {"sources_sha256": "d61dde3f79f20922cda206e86396fa511cf82dbdd212dfc32ad21dc70ad8ec0d", "bytes": 44956672 + 1562368},
+    "uniform": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 323249664 + 14190080},
+    "varlen": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 556992256 + 18768896},
+    "fp8spec": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 310369536 + 9145856},
+    "window": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 44958976 + 1689600},
 }
 
 
