@@ -96,7 +96,10 @@ struct Misc {
   // tile ahead of the correction and of the P.V, never two
   uint64_t pv_ready[2];   // leader: one arrival per CTA, P written and O corrected for the next P.V
   uint64_t pv_local[2];   // this CTA's 4 softmax + 4 correction warps, forwarded to the leader's pv_ready
-  uint64_t tail_ready;    // leader: the peer zeroed the tail of a request's last key group (one arrival a slot)
+  // leader: the peer zeroed the tail of a request's last key group (one arrival a slot); two,
+  // alternating by tail group, so the peer (at most a ring ahead of the MMA, and tail groups
+  // a tile's fills apart) can never complete a phase the MMA has not yet waited for
+  uint64_t tail_ready[2];
   uint64_t o_done[2];     // P.V of a tile complete
   uint64_t cor_ready[2];  // softmax -> correction: the tile's rescale factor is posted
   uint64_t tail_bar[2], xchg_bar;  // tail_bar: one per loader warp
@@ -269,10 +272,11 @@ __device__ __noinline__ void drain_after_abort(Misc& M, uint32_t rank, int warp,
 // `own`): each CTA landed the group locally on its tail barrier; wait for it, zero the
 // slots' rows past the length (any bits there, NaN included, must not reach P.V), then
 // the leader completes its slots' phases and the peer reports on the leader's
-// tail_ready (the MMA waits for both on this group).  Out of line: once per piece.
+// tail_ready[tg & 1], tg the CTA's tail groups so far (the MMA waits for both on this
+// group).  Out of line: once per piece.
 template <bool E4M3>
 __device__ __noinline__ bool tail_group(Misc& M, uint8_t* smem, int own, uint32_t rank, int lane, uint32_t tph,
-                                        int slot0, int slot1, bool mine0, bool mine1, int tail_rows) {
+                                        uint32_t tg, int slot0, int slot1, bool mine0, bool mine1, int tail_rows) {
   using C = Cfg<E4M3>;
   if (!kwait(M, smem_addr(&M.tail_bar[own]), tph & 1)) return false;
   if (lane == 0) M.ntail_done[own] += 1;
@@ -294,7 +298,7 @@ __device__ __noinline__ bool tail_group(Misc& M, uint8_t* smem, int own, uint32_
       if (rank == 0)
         mbar_arrive(smem_addr(&M.full[slot]));
       else
-        mbar_arrive_cluster(map_to_rank(smem_addr(&M.tail_ready), 0));
+        mbar_arrive_cluster(map_to_rank(smem_addr(&M.tail_ready[tg & 1]), 0));
     }
   }
   __syncwarp();
@@ -546,7 +550,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&M.o_done[i]), 1);
       mbar_init(smem_addr(&M.cor_ready[i]), 4);
     }
-    mbar_init(smem_addr(&M.tail_ready), C::kVItems);
+    mbar_init(smem_addr(&M.tail_ready[0]), C::kVItems);
+    mbar_init(smem_addr(&M.tail_ready[1]), C::kVItems);
     mbar_init(smem_addr(&M.tail_bar[0]), 1);
     mbar_init(smem_addr(&M.tail_bar[1]), 1);
     mbar_init(smem_addr(&M.xchg_bar), 4);
@@ -911,7 +916,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!take(va[it], slot[it])) return false;
           if (4 * tile + vp == ngroups - 1 && tail_rows != 0) {
             // the request's last key group: the peer zeroed its slots' tail too
-            if (!kwait(M, smem_addr(&M.tail_ready), tcount & 1)) return false;
+            if (!kwait(M, smem_addr(&M.tail_ready[tcount & 1]), (tcount >> 1) & 1)) return false;
             ++tcount;
           }
           tc_fence_after();
@@ -993,6 +998,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int32_t* table = &M.boxes[own][0][0];
     int fill = 0;
     uint32_t tph = 0;
+    uint32_t ntg = 0;  // tail groups so far (this warp's or not): their tail_ready barrier
     bool ok = true;
     // the next fill in consumption order: this warp's (wait until its slot is free) or the
     // other warp's (skip); lane-uniform
@@ -1088,7 +1094,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!acquire(slot[it], mine[it])) return false;
           nmine += mine[it] ? 1 : 0;
         }
-        const bool tail = 4 * tile + vp == ngroups - 1 && tail_rows != 0 && nmine != 0;
+        const bool tail_grp = 4 * tile + vp == ngroups - 1 && tail_rows != 0;
+        const bool tail = tail_grp && nmine != 0;
         // this CTA's 128-byte column blocks of V: bf16 blocks {0,1,4,5} or {2,3,6,7}
         // (two per slot, one slot per output chunk), e4m3 blocks {rank, 2 + rank}
         const uint32_t tbar = smem_addr(&M.tail_bar[own]);
@@ -1117,11 +1124,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (tail) {
-          if (!tail_group<E4M3>(M, smem, own, rank, lane, tph, slot[0], slot[C::kVItems - 1], mine[0],
+          if (!tail_group<E4M3>(M, smem, own, rank, lane, tph, ntg, slot[0], slot[C::kVItems - 1], mine[0],
                                 mine[C::kVItems - 1], tail_rows))
             return false;
           ++tph;
         }
+        if (tail_grp) ++ntg;
       }
       return true;
     };

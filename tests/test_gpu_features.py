@@ -90,6 +90,29 @@ def test_page_sizes_all_rows(P, dtype):
     compare(dtype, O, L, *oracle.decode(prob.host_inputs()))
 
 
+@pytest.mark.parametrize("P,dtype,clusters", [(8, "bf16", 1), (16, "e4m3", 3), (32, "bf16", 3), (64, "e4m3", 2),
+                                              (128, "bf16", 5)])
+def test_many_pieces_per_cluster_all_rows(P, dtype, clusters):
+    """Few clusters over many short and long rows: every cluster walks many pieces, so the
+    load and MMA pipeline crosses piece boundaries (the next piece's K ahead of the last
+    piece's V, the page boxes of both pieces held at once) and rows are cut at the shares'
+    ends."""
+    lens = [1 + (53 * i) % 700 for i in range(24)] + [2300, 0, 64, 65]
+    prob = wl.make_problem("uniform", seed=909, H=64, Sq=3, causal=True, dtype=dtype, page_size=P, seq_lens=lens)
+    O, L = host(*run(prob, num_clusters=clusters))
+    compare(dtype, O, L, *oracle.decode(prob.host_inputs()))
+
+
+@pytest.mark.parametrize("P,dtype", [(64, "bf16"), (16, "e4m3")])
+def test_segment_lists_past_shared_memory_all_rows(P, dtype):
+    """600 short rows on 2 clusters: about 300 pieces per cluster, more than the 192 segments
+    kept in shared memory (the rest are read from the workspace), one pipeline across all."""
+    lens = [1 + (97 * i) % 300 for i in range(600)]
+    prob = wl.make_problem("uniform", seed=919, H=128, Sq=1, dtype=dtype, page_size=P, seq_lens=lens)
+    O, L = host(*run(prob, num_clusters=2))
+    compare(dtype, O, L, *oracle.decode(prob.host_inputs()))
+
+
 @pytest.mark.parametrize("P,dtype", [(8, "bf16"), (32, "e4m3"), (256, "bf16")])
 def test_debug_gather_page_sizes_byte_exact(P, dtype):
     prob = wl.make_problem("uniform", seed=3, H=1, dtype=dtype, page_size=P, seq_lens=[100, 257, 64, 1, 0, 130])
