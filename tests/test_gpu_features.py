@@ -144,6 +144,29 @@ def test_local_visible_lens_all_rows(H, window, dtype):
     compare(dtype, O, L, *oracle.decode_ex(prob.host_inputs(), local_visible_lens=lvl))
 
 
+@pytest.mark.parametrize("dtype,P,clusters,window", [("bf16", 64, 2, -1), ("e4m3", 32, 3, 200), ("bf16", 16, 1, 500)])
+def test_local_visible_lens_few_clusters_all_rows(dtype, P, clusters, window):
+    """Per-token local bounds with many pieces per cluster (the loop-over-tokens spans)."""
+    lens = [1 + (71 * i) % 900 for i in range(16)] + [3000]
+    Sq = 4
+    prob = wl.make_problem("uniform", seed=313, H=32, Sq=Sq, causal=False, window_left=window, dtype=dtype,
+                           page_size=P, seq_lens=lens)
+    g = torch.Generator().manual_seed(6)
+    lvl = torch.stack([torch.randint(0, K + 40, (Sq,), generator=g) for K in lens]).to(torch.int32)
+    O, L = host(*run(prob, num_clusters=clusters, local_visible_lens=lvl.cuda()))
+    compare(dtype, O, L, *oracle.decode_ex(prob.host_inputs(), local_visible_lens=lvl))
+
+
+@pytest.mark.parametrize("dtype,H,Sq,clusters", [("bf16", 128, 4, 3), ("e4m3", 64, 3, 2), ("bf16", 16, 8, 1)])
+def test_in_kernel_combine_few_clusters_all_rows(dtype, H, Sq, clusters):
+    """The in-kernel combine with many pieces per cluster, bands of clusters (Sq x H > 128)
+    and packed rows."""
+    lens = [1 + (89 * i) % 1200 for i in range(12)] + [4100, 0]
+    prob = wl.make_problem("uniform", seed=323, H=H, Sq=Sq, causal=True, window_left=700, dtype=dtype, seq_lens=lens)
+    O, L = host(*run(prob, num_clusters=clusters, combine_in_kernel=True))
+    compare(dtype, O, L, *oracle.decode(prob.host_inputs()))
+
+
 def test_debug_mask_local_visible_lens_bit_exact():
     lens = [0, 1, 31, 33, 257]
     Sq, max_k = 3, 300
@@ -168,8 +191,8 @@ DCP = {
 }
 
 
-@pytest.mark.parametrize("name", list(DCP))
-def test_context_parallel_ranks_and_gpu_merge(name):
+@pytest.mark.parametrize("name,clusters", [(k, 0) for k in DCP] + [("w3_i5_sq4_window", 2), ("w2_i64_sq2_causal", 1)])
+def test_context_parallel_ranks_and_gpu_merge(name, clusters):
     c = DCP[name]
     prob = wl.make_problem("uniform", seed=404, H=c["H"], Sq=c["Sq"], causal=c["causal"], window_left=c["window"],
                            seq_lens=c["lens"])
@@ -177,7 +200,7 @@ def test_context_parallel_ranks_and_gpu_merge(name):
     for r in range(c["world"]):
         sh = wl.dcp_shard(prob, c["world"], r, c["inter"], seed=1)
         gsl = sh.extra["global_seq_lens"]
-        out, lse = run(sh, out_dtype=torch.float32, global_seq_lens=gsl.cuda())
+        out, lse = run(sh, out_dtype=torch.float32, global_seq_lens=gsl.cuda(), num_clusters=clusters)
         # this rank's share against the oracle's share
         O, L = host(out, lse)
         compare("bf16", O, L, *oracle.decode_ex(sh.host_inputs(), cp_world=c["world"], cp_rank=r,
