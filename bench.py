@@ -77,7 +77,7 @@ def describe(prob) -> str:
     lens = prob.seq_lens.tolist()
     klen = f"K={lens[0]}" if len(set(lens)) == 1 else f"K log-uniform [1,{w.max_len}] (sum {sum(lens)})"
     extra = (" causal" if w.causal else "") + (f" window_left={w.window_left}" if w.window_left >= 0 else "")
-    return f"{w.name}: B={w.B} H={w.H} Sq={w.Sq} {klen}{extra} {w.dtype} page_size=64 pool={prob.pool_pages} pages"
+    return f"{w.name}: B={w.B} H={w.H} Sq={w.Sq} {klen}{extra} {w.dtype} page_size={w.page_size} pool={prob.pool_pages} pages"
 
 
 def algorithmic_counts(prob):
@@ -250,7 +250,7 @@ def measure(name, args, world, rank, local_rank, peaks, peak_src):
     # --compact-pool: only the pages the batch uses (profiling: the same tiles and traffic in a
     # pool small enough to capture); the default keeps the workload's own pool
     prob = wl.make_problem(name, seed=rank_seed(wl.WORKLOADS[name].seed, rank),
-                           pool_pages=0 if args.compact_pool else None)
+                           pool_pages=0 if args.compact_pool else None, page_size=args.page_size or None)
     d = prob.device_inputs("cuda")
     dec = decoder_for(prob, **decode_options(args, prob))
     flops, kv = algorithmic_counts(prob)
@@ -330,7 +330,60 @@ def measure(name, args, world, rank, local_rank, peaks, peak_src):
         b.record(stream)
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
-    e2e_ms = max_over_ranks(statistics.mean(e_ms))
+    e2e_serial_ms = max_over_ranks(statistics.mean(e_ms))
+
+    # The same steps pipelined as a serving loop runs them: step i's H2D on a copy-in stream,
+    # its decode on the compute stream once they land, its D2H on a copy-out stream after
+    # it, two sets of buffers, so step i + 1's H2D and step i - 1's D2H overlap step i's
+    # decode.  Timed over all steps as a whole (events on the copy streams), with no L2 flush
+    # between steps; reported where the batch's KV is larger than L2 (129 MB), so that no
+    # step finds its KV left in L2 by the one before.
+    e2e_mode = "serial: each step's H2D, decode and D2H in turn, L2 flushed before each step"
+    e2e_ms = e2e_serial_ms
+    if kv > 129e6:
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        sets = []
+        for _ in range(2):
+            sets.append(dict(dq=[torch.empty_like(t) for t in dq], out=torch.empty_like(out),
+                             lse=torch.empty_like(lse), h_out=torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
+                             h_lse=torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)))
+
+        def pipelined(n):
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            done_in = [torch.cuda.Event() for _ in range(n)]
+            done_dec = [torch.cuda.Event() for _ in range(n)]
+            done_out = [torch.cuda.Event() for _ in range(n)]
+            start.record(s_in)
+            s_out.wait_event(start)
+            stream.wait_event(start)
+            for i in range(n):
+                b = sets[i & 1]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(done_dec[i - 2])  # set i & 1 no longer read
+                    for h, dv in zip(hq, b["dq"]):
+                        dv.copy_(h, non_blocking=True)
+                    done_in[i].record(s_in)
+                stream.wait_event(done_in[i])
+                if i >= 2:
+                    stream.wait_event(done_out[i - 2])  # set i & 1's outputs read back
+                dec(b["dq"][0], b["dq"][1], d["ckv"], d["kpe"], b["dq"][2], b["dq"][3], d["scale"], out=b["out"],
+                    lse=b["lse"], stream=stream)
+                done_dec[i].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done_dec[i])
+                    b["h_out"].copy_(b["out"], non_blocking=True)
+                    b["h_lse"].copy_(b["lse"], non_blocking=True)
+                    done_out[i].record(s_out)
+            s_out.wait_event(done_in[n - 1])
+            end.record(s_out)
+            end.synchronize()
+            return start.elapsed_time(end) / n
+
+        pipelined(max(2, args.warmup))
+        e2e_ms = max_over_ranks(pipelined(args.steps))
+        e2e_mode = ("pipelined: step i+1's H2D and step i-1's D2H on copy streams overlap step i's decode "
+                    "(two buffer sets), timed over all steps, no L2 flush (the KV is larger than L2)")
 
     # the same device-resident call back to back with no L2 flush between calls (part of
     # the KV can then still be in L2 from the previous call): reported beside the number
@@ -371,7 +424,8 @@ def measure(name, args, world, rank, local_rank, peaks, peak_src):
            "flops_per_step": flops, "kv_bytes_per_step": kv, "dtype": prob.w.dtype, "roofline": roof,
            "clocks": clk.summary(),
            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                   "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "mode": e2e_mode,
+                   "serial": {"value": world * flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms}},
            "no_flush": {"us_per_call": nf_ms * 1e3, "l2": "not flushed between calls"},
            "gpu_launches": launches_per_call * args.steps, "ms": ms}
     del d, dec, flush, out, lse, hq, dq
@@ -438,6 +492,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
     ap.add_argument("--partial-fp16", action="store_true", help="fp16 split partials for bf16 caches too")
     ap.add_argument("--num-clusters", type=int, default=0, help="CTA pairs of the split-KV launch (0: the planner's)")
+    ap.add_argument("--page-size", type=int, default=0, help="keys per KV page (0: the workload's, 64)")
     ap.add_argument("--no-pdl", action="store_true", help="launch the reduction without programmatic dependent launch")
     ap.add_argument("--combine-in-kernel", action="store_true",
                     help="combine split rows inside the split-KV kernel instead of in the reduction kernel")
