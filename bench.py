@@ -235,6 +235,8 @@ def decode_options(args, prob) -> dict:
     opts = {"use_pdl": not args.no_pdl, "combine_in_kernel": args.combine_in_kernel}
     if args.num_clusters:
         opts["num_clusters"] = args.num_clusters
+    if args.reducer_d_tiles:
+        opts["reducer_d_tiles"] = args.reducer_d_tiles
     if args.partial_fp16:
         opts["partial_fp16"] = True
     return opts
@@ -493,6 +495,7 @@ def main():
     ap.add_argument("--partial-fp16", action="store_true", help="fp16 split partials for bf16 caches too")
     ap.add_argument("--num-clusters", type=int, default=0, help="CTA pairs of the split-KV launch (0: the planner's)")
     ap.add_argument("--page-size", type=int, default=0, help="keys per KV page (0: the workload's, 64)")
+    ap.add_argument("--reducer-d-tiles", type=int, default=0, help="reduction CTAs per work row across the dims (0: 8)")
     ap.add_argument("--no-pdl", action="store_true", help="launch the reduction without programmatic dependent launch")
     ap.add_argument("--combine-in-kernel", action="store_true",
                     help="combine split rows inside the split-KV kernel instead of in the reduction kernel")
