@@ -237,8 +237,8 @@ def decode_options(args, prob) -> dict:
         opts["num_clusters"] = args.num_clusters
     if args.reducer_d_tiles:
         opts["reducer_d_tiles"] = args.reducer_d_tiles
-    if args.partial_fp16:
-        opts["partial_fp16"] = True
+    if args.fp32_partials:
+        opts["partial_fp16"] = False
     return opts
 
 
@@ -492,7 +492,7 @@ def main():
                     help="all (default): the uniform headline plus records for varlen, fp8spec and window")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline (0: skip)")
-    ap.add_argument("--partial-fp16", action="store_true", help="fp16 split partials for bf16 caches too")
+    ap.add_argument("--fp32-partials", action="store_true", help="fp32 split partials (default: fp16, scaled)")
     ap.add_argument("--num-clusters", type=int, default=0, help="CTA pairs of the split-KV launch (0: the planner's)")
     ap.add_argument("--page-size", type=int, default=0, help="keys per KV page (0: the workload's, 64)")
     ap.add_argument("--reducer-d-tiles", type=int, default=0, help="reduction CTAs per work row across the dims (0: 8)")

@@ -100,10 +100,11 @@ typedef enum { MLA_BF16 = 0, MLA_E4M3 = 1, MLA_F32 = 2 } mla_dtype_t;
  *                     above the window floor, when a window is set); it replaces the causal
  *                     bound.  NULL: the causal flag decides.
  *  partial_fp16       1: store the split pieces' normalized partial outputs as fp16
- *                     (__init__'s partial_fp16) instead of fp32: half the reduction's
- *                     bytes.  The partials hold O / l in units of the stored value codes,
- *                     so every |ckv| code must stay within the fp16 range (always true for
- *                     e4m3 codes, |x| <= 448; the caller's promise for bf16 caches).
+ *                     (__init__'s partial_fp16) instead of fp32: half the bytes written by
+ *                     the split-KV kernel and read by the reduction.  Each (row, half of
+ *                     the dims) is scaled by a power of two that puts its largest |value|
+ *                     in [2^14, 2^15), so any finite value fits (fp16's 11 significant bits
+ *                     each, in a sum rounded to the output type afterwards).
  *  reducer_d_tiles    CTAs per work row across the 512 output dims in the reduction:
  *                     1, 2, 4 or 8 (0: 8)
  *  use_pdl            1: launch the reduction with programmatic dependent launch, so its

@@ -33,9 +33,10 @@ class PagedMlaDecoder:
                  kv_descale: float = 1.0, num_clusters: int = 0, page_size: int = PAGE_SIZE, cp_world: int = 1,
                  cp_rank: int = 0, cp_interleave: int = 1, partial_fp16=None, reducer_d_tiles: int = 0,
                  use_pdl: bool = True, combine_in_kernel: bool = False, device="cuda"):
-        # fp16 partials by default where the stored value codes always fit fp16 (e4m3, |x| <= 448)
+        # fp16 partials (scaled per row and half of the dims, so any value fits) unless the
+        # output is fp32, whose precision the fp32 partials keep
         if partial_fp16 is None:
-            partial_fp16 = qkv_dtype == torch.float8_e4m3fn
+            partial_fp16 = out_dtype != torch.float32
         self.H, self.Sq = H, seq_len_q
         self.window_left = window_left
         self.out_dtype = out_dtype

@@ -190,9 +190,13 @@ __host__ __device__ inline long long tile_unit(long long start, int pu, int i) {
 
 // -------------------------------------------------------------- workspace
 // [header 256 B][cta_status 2G][row_info Rw][overflow segments 2G x max(0, S - kSmemSegs)]
-// [partial_lse slots x 128 fp32][partial_o slots x 128 x 512, fp32 or fp16]
+// [partial_lse slots x 128 fp32][fp16: partial_scale slots x 2 x 128 fp32]
+// [partial_o slots x 128 x 512, fp32 or fp16]
 // A slot's O is laid out [dim / V][row][dim % V] with V = 4 (fp32) or 8 (fp16): a warp's
-// 16-byte store (V dims of 32 consecutive rows) is 512 contiguous bytes.
+// 16-byte store (V dims of 32 consecutive rows) is 512 contiguous bytes.  fp16 partials
+// are scaled by a power of two per (row, half of the dims: 256 c + 128 h + [0, 128)) so the
+// half's largest |value| lands in [2^14, 2^15): any finite value fits, with fp16's 11 bits;
+// partial_scale holds the base-2 exponent that undoes it.
 // Every CTA of the split-KV kernel overwrites its own status word on every call and the
 // schedule rewrites the header and row table, so the workspace needs no clearing.
 struct WsHeader {
@@ -233,7 +237,7 @@ constexpr int kMaxClusters = 1024;  // the partial slot of a segment has 18 bits
 __host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t cta_status, row_info, counters, segs, partial_lse, partial_o, total;
+  size_t cta_status, row_info, counters, segs, partial_lse, partial_scale, partial_o, total;
   size_t slot_bytes;  // bytes of one slot's O
   int seg_cap;        // overflow segments per CTA
 };
@@ -257,6 +261,8 @@ __host__ __device__ inline WsLayout ws_layout(int B, int Sq, int H, int G, int p
   off = align256(off + sizeof(Segment) * 2 * (size_t)G * (size_t)l.seg_cap);
   l.partial_lse = off;
   off = align256(off + sizeof(float) * (size_t)d.slots * kTileM);
+  l.partial_scale = off;  // fp16: [slot][half][row]
+  if (partial_f16) off = align256(off + sizeof(float) * (size_t)d.slots * 2 * kTileM);
   l.partial_o = off;
   off = align256(off + l.slot_bytes * (size_t)d.slots);
   l.total = off;

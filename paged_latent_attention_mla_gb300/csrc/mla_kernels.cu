@@ -28,7 +28,7 @@ namespace mla {
 // transposes each 64-dim chunk through shared memory and writes the output row-major.
 // Work rows written whole by the split-KV kernel (one piece) are skipped.
 template <bool F16>
-__global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256, 2) reduce_kernel(const DecodeParams p) {
   grid_dependency_wait();  // the split-KV kernel's partials (programmatic dependent launch)
   __shared__ float tile[kTileM][64 + 1];  // [row][dim], padded against bank conflicts
   const int w = blockIdx.y;
@@ -44,10 +44,14 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
   const float* plse = reinterpret_cast<const float*>(p.ws + L.partial_lse) + m;
   const uint8_t* po = p.ws + L.partial_o;
   auto slot_of = [&](int i) { return (size_t)ri.first_slot + (size_t)i * d.wb; };
-  // 32 dims of piece i from d0 into x
-  auto load = [&](int i, int d0, float (&x)[32]) {
+  // fp16 partials carry a power-of-two scale per (row, half of each 256-dim chunk); a
+  // thread's 32 dims lie in one half
+  const float* pscale = reinterpret_cast<const float*>(p.ws + L.partial_scale) + m;
+  // 32 dims of piece i from d0 into x, and their scale exponent (loaded with them)
+  auto load = [&](int i, int d0, float (&x)[32], float& sc) {
     const size_t sl = slot_of(i);
     if constexpr (F16) {
+      sc = pscale[(sl * 2 + ((d0 >> 7) & 1)) * kTileM];
       const uint4* src = reinterpret_cast<const uint4*>(po + sl * L.slot_bytes) + m;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -61,6 +65,7 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
         }
       }
     } else {
+      sc = 0.f;
       const float4* src = reinterpret_cast<const float4*>(po + sl * L.slot_bytes) + m;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -75,10 +80,10 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
   const int band = kDLatent / p.reduce_d_tiles;
   // the first round's partials (pieces 0 and 1 of the first chunk) go out with the LSE
   // loads, before the LSE arithmetic: one dependent round trip fewer
-  float x[2][32];
+  float x[2][32], xs[2] = {0.f, 0.f};
   if (np > 0) {
-    load(0, blockIdx.x * band + 32 * dg, x[0]);
-    load(np > 1 ? 1 : 0, blockIdx.x * band + 32 * dg, x[1]);
+    load(0, blockIdx.x * band + 32 * dg, x[0], xs[0]);
+    load(np > 1 ? 1 : 0, blockIdx.x * band + 32 * dg, x[1], xs[1]);
   }
   // the pieces' LSEs: max, sum, the row's LSE
   float mx = -INFINITY;
@@ -87,9 +92,9 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
   float sum = 0.f;
   for (int i = 0; i < np; ++i) sum += exp2f(plse[slot_of(i) * kTileM] - m0);
   const float lse2 = sum > 0.f ? m0 + log2f(sum) : -INFINITY;
-  auto weight = [&](int i) {
+  auto weight = [&](int i, float sc) {
     const float li = plse[slot_of(i) * kTileM];
-    return (sum > 0.f && li != -INFINITY) ? exp2f(li - lse2) * p.ckv_descale : 0.f;
+    return (sum > 0.f && li != -INFINITY) ? exp2f(li - lse2 + sc) * p.ckv_descale : 0.f;
   };
   for (int c = 0; c < band / 64; ++c) {
     const int d0 = blockIdx.x * band + 64 * c + 32 * dg;  // this thread's 32 dims
@@ -101,11 +106,11 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeParams p) {
     for (int i0 = 0; i0 < np; i0 += 2) {
       if (c > 0 || i0 > 0) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) load(i0 + u < np ? i0 + u : i0, d0, x[u]);
+        for (int u = 0; u < 2; ++u) load(i0 + u < np ? i0 + u : i0, d0, x[u], xs[u]);
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const float wt = i0 + u < np ? weight(i0 + u) : 0.f;
+        const float wt = i0 + u < np ? weight(i0 + u, xs[u]) : 0.f;
         if (wt == 0.f) continue;
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] += wt * x[u][e];

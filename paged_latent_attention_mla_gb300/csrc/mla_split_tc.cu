@@ -345,8 +345,8 @@ __device__ __noinline__ int arrive_piece(Misc& M, const DecodeParams& p, unsigne
 // threads (a multiple of 64), t this one: M row 64 rank + (t & 63), 32-column blocks
 // t / 64 + k nthr / 64; two pieces' loads are issued before either is applied.
 __device__ __noinline__ void combine_row(const DecodeParams& p, const uint8_t* part_o, const float* part_lse,
-                                         size_t slot_bytes, int w, int first_slot, int np, int wb, int Qb,
-                                         uint32_t rank, int t, int nthr) {
+                                         const float* part_scale, size_t slot_bytes, int w, int first_slot, int np,
+                                         int wb, int Qb, uint32_t rank, int t, int nthr) {
   __threadfence();  // the other pieces' stores, published before their arrivals
   const int rows_q = p.Sq * p.H;
   const int m = 64 * (int)rank + (t & 63);
@@ -400,9 +400,12 @@ __device__ __noinline__ void combine_row(const DecodeParams& p, const uint8_t* p
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const float li = i0 + u < np ? __ldcg(plse + (size_t)(first_slot + (i0 + u) * wb) * kTileM) : -INFINITY;
+        const size_t sl = (size_t)(first_slot + (i0 + u) * wb);
+        const float li = i0 + u < np ? __ldcg(plse + sl * kTileM) : -INFINITY;
         if (!(sum > 0.f) || li == -INFINITY) continue;
-        const float wt = exp2f(li - lse2) * p.ckv_descale;
+        // fp16 partials: undo the half's power-of-two scale (d0's half of its 256-dim chunk)
+        const float sc = p.partial_f16 ? __ldcg(part_scale + (sl * 2 + ((d0 >> 7) & 1)) * kTileM + m) : 0.f;
+        const float wt = exp2f(li - lse2 + sc) * p.ckv_descale;
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] += wt * x[u][e];
       }
@@ -453,9 +456,9 @@ __device__ __noinline__ void write_empty_rows(const DecodeParams& p, const DealS
 // the base-2 LSE, combined and scaled by the reduction kernel).  A row with no visible
 // key in the piece gets O = 0 and LSE = -inf.  TMEM columns [128 c', +128) of this lane
 // hold D columns 256 c' + 128 half + [0, 128).  Out of line: it runs once per piece.
-__device__ __noinline__ void piece_epilogue(const DecodeParams& p, uint8_t* slot_o, float* slot_lse, uint32_t obase,
-                                            int half, int m, int b, int flat, bool live, bool direct, float lrow,
-                                            float mrow) {
+__device__ __noinline__ void piece_epilogue(const DecodeParams& p, uint8_t* slot_o, float* slot_lse, float* slot_scale,
+                                            uint32_t obase, int half, int m, int b, int flat, bool live, bool direct,
+                                            float lrow, float mrow) {
   const bool empty = !(lrow > 0.f);
   const int rows_q = p.Sq * p.H;
   if (direct) {
@@ -483,8 +486,26 @@ __device__ __noinline__ void piece_epilogue(const DecodeParams& p, uint8_t* slot
     }
     if (live && half == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : (mrow + log2f(lrow)) * 0.69314718055994530942f;
   } else {
-    const float inv = empty ? 0.f : 1.f / lrow;
+    float inv = empty ? 0.f : 1.f / lrow;
     uint8_t* so = slot_o;
+    if (p.partial_f16) {
+      // this thread's power-of-two scale: the largest |O / l| of its 256 dims to [2^14, 2^15)
+      float amax = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[32];
+        tmem_ld32(obase + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(u2f(r[e])));
+      }
+      amax *= inv;
+      int ex = 0;
+      if (amax > 0.f && amax <= 3.0e38f) frexpf(amax, &ex);  // amax = f 2^ex, f in [0.5, 1)
+      const int sh = amax > 0.f && amax <= 3.0e38f ? ex - 15 : 0;
+      inv = ldexpf(inv, -sh);
+      if (live) slot_scale[half * kTileM + m] = (float)sh;
+    }
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       uint32_t r[32];
@@ -834,7 +855,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int slot = sg.slot();
       const size_t sl = slot < 0 ? 0 : (size_t)slot;
       piece_epilogue(p, p.ws + WL.partial_o + sl * WL.slot_bytes,
-                     reinterpret_cast<float*>(p.ws + WL.partial_lse) + sl * kTileM, obase, half, m, b, flat,
+                     reinterpret_cast<float*>(p.ws + WL.partial_lse) + sl * kTileM,
+                     reinterpret_cast<float*>(p.ws + WL.partial_scale) + sl * 2 * kTileM, obase, half, m, b, flat,
                      flat < rows_q, slot < 0, fl, fm);
       if (p.fused_combine && slot >= 0) {
         tc_fence_before();
@@ -846,8 +868,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = v >= 0;
         if (!ok) break;
         if (v > 0)
-          combine_row(p, p.ws + WL.partial_o, reinterpret_cast<const float*>(p.ws + WL.partial_lse), WL.slot_bytes,
-                      sg.row(), first, sg.n_parts(), DS.wb, DS.Qb, rank, L, 128);
+          combine_row(p, p.ws + WL.partial_o, reinterpret_cast<const float*>(p.ws + WL.partial_lse),
+                      reinterpret_cast<const float*>(p.ws + WL.partial_scale), WL.slot_bytes, sg.row(), first,
+                      sg.n_parts(), DS.wb, DS.Qb, rank, L, 128);
       }
       tc_fence_before();
     }
@@ -1200,8 +1223,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int n = min((int)M.ncl, kCombList);
     for (int e = 0; e < n; ++e) {
       const int4 E = M.comb_list[e];
-      combine_row(p, p.ws + WL.partial_o, reinterpret_cast<const float*>(p.ws + WL.partial_lse), WL.slot_bytes, E.x,
-                  E.y, E.z, DS.wb, DS.Qb, rank, tid, 256);
+      combine_row(p, p.ws + WL.partial_o, reinterpret_cast<const float*>(p.ws + WL.partial_lse),
+                  reinterpret_cast<const float*>(p.ws + WL.partial_scale), WL.slot_bytes, E.x, E.y, E.z, DS.wb, DS.Qb,
+                  rank, tid, 256);
     }
   }
 }

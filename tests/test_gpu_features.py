@@ -283,6 +283,19 @@ def test_combine_in_kernel_reuses_one_workspace_across_calls_and_shapes():
     assert torch.allclose(l_fused[fin], l_red[fin], rtol=0, atol=1e-4)
 
 
+@pytest.mark.parametrize("shift", [20, -30])
+def test_fp16_partials_hold_any_value_range(shift):
+    """The default fp16 partials with values far outside fp16's range (|O| ~ 2^20, beyond
+    65504) and far below it (~2^-30, fp16 subnormal): the per-(row, half) power-of-two scale
+    keeps them; rows cut into several pieces.  Scaling the latent cache by 2^shift and the
+    latent queries by 2^-shift (both exact in bf16) leaves the scores unchanged."""
+    prob = wl.make_problem("uniform", seed=515, H=128, Sq=1, seq_lens=[3000, 900, 17, 2048])
+    prob.ckv = prob.ckv * 2.0 ** shift
+    prob.q_latent = prob.q_latent * 2.0 ** -shift
+    O, L = host(*run(prob, num_clusters=12))
+    compare("bf16", O, L, *oracle.decode(prob.host_inputs()))
+
+
 def test_fp16_partials_e4m3_full_size():
     prob = wl.make_problem("fp8spec")
     O, L = host(*run(prob, partial_fp16=True))
