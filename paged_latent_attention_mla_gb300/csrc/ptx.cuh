@@ -269,19 +269,12 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t chunk
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
-}  // namespace mla
-
-namespace mla {
 // 64-byte-swizzled K-major operand (rows of 64 B, 8-row groups of 512 B)
 __host__ __device__ constexpr uint64_t smem_desc_sw64(uint32_t addr, uint32_t sbo_bytes) {
   return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1u) << 16) |
          (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
-__device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
-}  // namespace mla
-
-namespace mla {
 // Complete `bytes` of the pending transaction count of a barrier in this CTA without a
 // copy: accounts for bytes a copy that was never issued would have brought.
 __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
