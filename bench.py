@@ -49,10 +49,10 @@ ALL = ["uniform", "varlen", "fp8spec", "window"]
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 323249664 + 14190080},
-    "varlen": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 556992256 + 18768896},
-    "fp8spec": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 310369536 + 9145856},
-    "window": {"sources_sha256": "5135e2da15abe45a9f3c5ec5b027ac087d71f6319690e99e468348d26e5d89b8", "bytes": 44958976 + 1689600},
+    "uniform": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 321867264 + 8232448},
+    "varlen": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 556475136 + 15650560},
+    "fp8spec": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 310334208 + 9053952},
+    "window": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 44963072 + 1181696},
 }
 
 
