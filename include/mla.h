@@ -18,9 +18,11 @@
  * (the window_left docstring of __init__).  A row with no visible key gets
  * out = 0 and lse = -inf (write_empty_output).
  *
- * Work is split along the KV axis across the GPU; each piece writes a
- * normalized partial output and its log-sum-exp into the caller's workspace,
- * and a reduction combines them with weights 2^(lse_i - lse) (reduction_kernel).
+ * Work is split along the KV axis across the GPU.  A row cut into several pieces
+ * has each piece write a normalized partial output and its base-2 log-sum-exp
+ * into the caller's workspace, and a reduction combines them with weights
+ * 2^(lse_i - lse) (reduction_kernel): a second kernel, or the split kernel
+ * itself with combine_in_kernel.  A row in one piece is written directly.
  *
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers unless marked host.  The caller owns every
@@ -181,9 +183,10 @@ MLA_API mla_status_t mla_plan(const int32_t *seq_lens, int B, int H, int page_si
  *  window_left -1, or the sliding-window span (same value as given to mla_plan)
  *  out        [B, seq_len_q, H, 512] out_dtype
  *  lse        [B, seq_len_q, H] fp32 natural-log LSE, or NULL to skip it
- *  workspace  device scratch of at least the planned size, 256-byte aligned.  Zero it
- *             once after allocating it (its rows' arrival counters must start at zero or
- *             hold an earlier call's tag); after that it needs no clearing between calls
+ *  workspace  device scratch of at least the planned size, 256-byte aligned.  With
+ *             combine_in_kernel, zero it once after allocating it (the rows' arrival
+ *             counters must start at zero or hold an earlier call's tag); it needs no
+ *             clearing otherwise, nor between calls
  *  stream     the CUDA stream all work is enqueued on
  *
  * Cache slots past a request's length and pages no visible key uses may hold
