@@ -191,8 +191,13 @@ DCP = {
 }
 
 
-@pytest.mark.parametrize("name,clusters", [(k, 0) for k in DCP] + [("w3_i5_sq4_window", 2), ("w2_i64_sq2_causal", 1)])
-def test_context_parallel_ranks_and_gpu_merge(name, clusters):
+@pytest.mark.parametrize("name,clusters,out_dtype",
+                         [(k, 0, torch.float32) for k in DCP] +
+                         [("w3_i5_sq4_window", 2, torch.float32), ("w2_i64_sq2_causal", 1, torch.float32),
+                          ("w2_i64_sq2_causal", 3, torch.bfloat16), ("w4_i1_h16_sq3", 2, torch.bfloat16)])
+def test_context_parallel_ranks_and_gpu_merge(name, clusters, out_dtype):
+    """Every rank's share against the oracle's share, then the GPU merge against the whole
+    decode; fp32 shares (fp32 partials), and bf16 shares (fp16 partials, merged in bf16)."""
     c = DCP[name]
     prob = wl.make_problem("uniform", seed=404, H=c["H"], Sq=c["Sq"], causal=c["causal"], window_left=c["window"],
                            seq_lens=c["lens"])
@@ -200,7 +205,7 @@ def test_context_parallel_ranks_and_gpu_merge(name, clusters):
     for r in range(c["world"]):
         sh = wl.dcp_shard(prob, c["world"], r, c["inter"], seed=1)
         gsl = sh.extra["global_seq_lens"]
-        out, lse = run(sh, out_dtype=torch.float32, global_seq_lens=gsl.cuda(), num_clusters=clusters)
+        out, lse = run(sh, out_dtype=out_dtype, global_seq_lens=gsl.cuda(), num_clusters=clusters)
         # this rank's share against the oracle's share
         O, L = host(out, lse)
         compare("bf16", O, L, *oracle.decode_ex(sh.host_inputs(), cp_world=c["world"], cp_rank=r,
