@@ -597,11 +597,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // the batch schedule, in the ring memory before any tile lands there
     int32_t* scratch = reinterpret_cast<int32_t*>(smem + C::kOffRing);
     Sched sc = build_schedule(p, scratch, &M.err);
-    if (blockIdx.x * blockDim.x < DS.Rw) write_row_table(p, sc);  // the CTAs that own rows of the table
+    // this CTA's pieces first (every role waits for them), then the row table's share
+    // (measured: the other order held the segments back by 1.6 us)
     if (warp == 0) {
       const int nseg = build_segments(p, sc, cl, segs, overflow);
       if (lane == 0) M.nseg = nseg;
     }
+    if (blockIdx.x * blockDim.x < DS.Rw) write_row_table(p, sc);  // the CTAs that own rows of the table
   }
   __syncthreads();
   tc_fence_before();
