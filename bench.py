@@ -49,10 +49,10 @@ ALL = ["uniform", "varlen", "fp8spec", "window"]
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 321867264 + 8232448},
-    "varlen": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 556475136 + 15650560},
-    "fp8spec": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 310334208 + 9053952},
-    "window": {"sources_sha256": "97c64799e72b1dde4b10c97e08fcb68f7bbd9965ba96e073cce035c51278f755", "bytes": 44963072 + 1181696},
+    "uniform": {"sources_sha256": "ff9b61951a9e5bfe5104c7877bd80557567babb7e0874d8fd4da3a37ed932d39", "bytes": 321861888 + 8038144},
+    "varlen": {"sources_sha256": "ff9b61951a9e5bfe5104c7877bd80557567babb7e0874d8fd4da3a37ed932d39", "bytes": 556163328 + 15452416},
+    "fp8spec": {"sources_sha256": "ff9b61951a9e5bfe5104c7877bd80557567babb7e0874d8fd4da3a37ed932d39", "bytes": 310389504 + 9145344},
+    "window": {"sources_sha256": "ff9b61951a9e5bfe5104c7877bd80557567babb7e0874d8fd4da3a37ed932d39", "bytes": 44971264 + 784128},
 }
 
 
