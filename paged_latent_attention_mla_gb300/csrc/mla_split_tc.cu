@@ -9,7 +9,8 @@
 //   warps 0-3  softmax: online max / exp2 / row sums, P (bf16 or e4m3) into
 //              tensor memory over the S it came from (below)
 //   warps 4-7  correction: rescale O when the row max moves, final epilogue
-//   warp 8     MMA issue (leader CTA, one thread) and TMEM allocation
+//   warp 8     MMA issue (leader CTA, one thread) and TMEM allocation: QK^T(t + 1)
+//              then P.V(t) over all of the cluster's tiles, across pieces too
 //   warp 9     TMA loads of Q (once per piece of work)
 //   warps 10-11 TMA loads of K blocks and V pages into one ring of 16 KB slots,
 //              in exactly the order the MMAs consume them (even fills by warp 10,
@@ -26,8 +27,9 @@
 // (its token's causal, window or local bound, on this rank's keys under decode
 // context parallelism).  The split follows the batch schedule (schedule.cuh): a
 // work row cut into several pieces writes each to a workspace slot (fp32, or fp16
-// when asked) that the reduction kernel combines; a work row in one piece is
-// written to the output directly.  Every mbarrier wait is bounded: on timeout the
+// scaled by a power of two per row and half of the dims) that the reduction kernel
+// combines, or that the last of its pieces combines here (combine_in_kernel); a work
+// row in one piece is written to the output directly.  Every mbarrier wait is bounded: on timeout the
 // kernel records kErrTimeout, tells its peer CTA, unwinds its roles, and before
 // freeing tensor memory proves with bounded waits that every copy it issued has
 // landed and every MMA it issued has completed.
@@ -1011,12 +1013,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 10) {
     // ------------------------------------------------------------ K blocks and V key groups, one ring
-    // Consumption order of each piece: K(t0), then K(t), V(t - 1) for the following tiles,
-    // then V(last); a K block is this CTA's two key groups x 128 B of columns, a V key group
-    // this CTA's output columns of 64 keys.  Two warps issue the copies: warp 10 the even
-    // fills, warp 11 the odd ones.  The slot count is even, so a slot always has the same
-    // owner, and an owner only ever waits for the release of its own previous fill of the
-    // slot.  Lane k of the owning warp issues the tile's box k (page boxes: tma_pages.cuh).
+    // Consumption order over the CTA's tiles, across pieces: K(t0), then K(t), V(t - 1) for
+    // every following tile, then V(last); a K block is this CTA's two key groups x 128 B of
+    // columns, a V key group this CTA's output columns of 64 keys.  Two warps issue the
+    // copies: warp 10 the even fills, warp 11 the odd ones.  The slot count is even, so a
+    // slot always has the same owner, and an owner only ever waits for the release of its
+    // own previous fill of the slot.  Lane q of the owning warp issues box q of a fill
+    // (page boxes: tma_pages.cuh).
     const int own = warp - 10;
     const int nb = ONE_BOX ? 1 : boxes_per_group(p.page_size), br = ONE_BOX ? kKeyGroup : box_rows(p.page_size);
     constexpr bool one_box = ONE_BOX;
@@ -1034,12 +1037,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++fill;
       return true;
     };
-    // Page boxes of a tile, loaded a tile ahead into registers and used a tile later, so
-    // the page-table reads never stall the issuing lane (the validity check is a select and
-    // a bad page id is reported at the end of the piece).  page_size >= 64: one box per key
-    // group, every lane holds the four; below 64: lane k holds box k and writes its page to
-    // the warp's table when the tile comes up, where the issuing lane reads it.  Copies are
-    // issued by lane 0: the loader's per-fill latency is on the ring's critical path.
+    // Page boxes of a tile, loaded a tile ahead into registers and used a tile later (the
+    // validity check is a select, and a bad page id is reported at the end).  page_size >= 64:
+    // one box per key group, every lane holds the four; below 64: lane k holds box k and
+    // writes its page to the warp's table when the tile comes up, where the issuing lanes
+    // read it.
     struct TileBoxes {
       int pg[4], rw[4];
     };
