@@ -1191,9 +1191,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       TileBoxes cur, next;
       fetch(b, K, sg.tile_begin, cur);
       for (int tile = sg.tile_begin; tile < sg.tile_end && ok; ++tile, ++ti) {
-        if (tile + 1 < sg.tile_end) fetch(b, K, tile + 1, next);  // read a tile ahead
+        // the next tile's page ids: bf16, read once this tile's K copies are out (its first
+        // copy then waits only for its own page ids); e4m3, before them, a tile ahead of its
+        // L2 prefetch (each order measured faster for its type)
+        if (E4M3 && tile + 1 < sg.tile_end) fetch(b, K, tile + 1, next);
         publish(ti, cur);
         ok = load_k(ti, cur);
+        if (!E4M3 && tile + 1 < sg.tile_end) fetch(b, K, tile + 1, next);
         if (ok && tile + 1 < sg.tile_end) prefetch_k(next);
         if (ok && pend) ok = load_v(pend_tile, pend_ti, pend_ng, pend_tr, pend_tb);
         pend = true;
