@@ -49,10 +49,10 @@ ALL = ["uniform", "varlen", "fp8spec", "window"]
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "9e6d6a7ea7afc68cb2b987bcac30bbd656ffb5191e69a0be9f5920162e84dd29", "bytes": 321861888 + 8038144},
-    "varlen": {"sources_sha256": "9e6d6a7ea7afc68cb2b987bcac30bbd656ffb5191e69a0be9f5920162e84dd29", "bytes": 556163328 + 15452416},
-    "fp8spec": {"sources_sha256": "9e6d6a7ea7afc68cb2b987bcac30bbd656ffb5191e69a0be9f5920162e84dd29", "bytes": 310389504 + 9145344},
-    "window": {"sources_sha256": "9e6d6a7ea7afc68cb2b987bcac30bbd656ffb5191e69a0be9f5920162e84dd29", "bytes": 44971264 + 784128},
+    "uniform": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 322251008 + 8147968},
+    "varlen": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 558720000 + 15538176},
+    "fp8spec": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 310204928 + 8883200},
+    "window": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 44969472 + 767488},
 }
 
 
