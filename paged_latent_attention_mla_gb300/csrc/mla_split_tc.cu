@@ -845,9 +845,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&M.pv_local[st]));
         if (warp == 4) {
-          // forward this CTA's readiness to the leader: one cross-CTA arrive per tile
+          // forward this CTA's readiness to the leader: one cross-CTA arrive per tile.  P and
+          // the corrected O are in tensor memory (ordered by the writers' tcgen05 waits and
+          // fences), so the arrive need not release generic memory at cluster scope
           if (!(ok = kwait(M, smem_addr(&M.pv_local[st]), (j >> 1) & 1))) break;
-          if (lane == 0) mbar_arrive_cluster(lead(M.pv_ready[st]));
+          if (lane == 0) mbar_arrive_remote(lead(M.pv_ready[st]));
           __syncwarp();
         }
       }
