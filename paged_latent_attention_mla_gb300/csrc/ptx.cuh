@@ -62,17 +62,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-// arrive on a barrier given by its shared::cluster address (own or peer CTA), releasing
-// this thread's prior writes at cluster scope.  Costly under load: measured on an SM with a
-// ring of TMA copies in flight, each such arrive held its thread about 0.6 us, so it is
-// kept off the per-tile path.
+// Arrive on a barrier given by its shared::cluster address (own or peer CTA), releasing
+// this thread's prior writes at cluster scope (for generic-memory data the other CTA's side
+// depends on).  It waits for the SM's outstanding memory operations: measured on an SM with
+// a ring of TMA copies in flight, it held its thread 1.8 us (0.16 us idle).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-// The same arrive with the default semantics (release at CTA scope), for an event that
-// carries no generic-memory data to the other CTA: tensor-memory writes are ordered by
-// tcgen05.wait::st and the tcgen05 thread-sync fences on either side of the barrier.
+// The same arrive with the default semantics (release at CTA scope: 4 ns under the same
+// load), for an event that carries no generic-memory data to the other CTA: tensor-memory
+// writes are ordered by tcgen05.wait::st and the tcgen05 thread-sync fences around it.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
