@@ -49,10 +49,10 @@ ALL = ["uniform", "varlen", "fp8spec", "window"]
 # the kernel sources it was taken on: reported when their hash still matches, else null.
 KERNEL_SOURCES = ("mla_split_tc.cu", "mla_common.cuh", "schedule.cuh", "tma_pages.cuh", "ptx.cuh")
 NCU_TRAFFIC = {
-    "uniform": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 322251008 + 8147968},
-    "varlen": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 558720000 + 15538176},
-    "fp8spec": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 310204928 + 8883200},
-    "window": {"sources_sha256": "e3e6f1af2b13e85a227ef5c9ce6755bd507ac14bcc51ef4bd9d72689b22e7237", "bytes": 44969472 + 767488},
+    "uniform": {"sources_sha256": "c1995718be5b00232ab7e8a732b698b787ec4bb01a2a2cb8fee52dd4cf344551", "bytes": 322160896 + 7964416},
+    "varlen": {"sources_sha256": "c1995718be5b00232ab7e8a732b698b787ec4bb01a2a2cb8fee52dd4cf344551", "bytes": 558129152 + 15618560},
+    "fp8spec": {"sources_sha256": "c1995718be5b00232ab7e8a732b698b787ec4bb01a2a2cb8fee52dd4cf344551", "bytes": 310328064 + 8987648},
+    "window": {"sources_sha256": "c1995718be5b00232ab7e8a732b698b787ec4bb01a2a2cb8fee52dd4cf344551", "bytes": 44969984 + 766976},
 }
 
 
